@@ -1,0 +1,172 @@
+/*
+ * Batched row-wise top-k selection on GB300 (sm_103a): the C ABI.
+ *
+ * The operation.  For every row r of a row-major fp32 score matrix, return the
+ * k largest of the row's first L_r scores together with their in-row int32
+ * indices, ordered by value descending; equal values go to the smaller index.
+ * This is the selection a sparse-attention indexer runs for each query token
+ * to decide which cached positions attention reads: "find the biggest 512
+ * numbers in a list of a million" (The Secret GPU Kernel Behind DeepSeek V4.1
+ * Flash, video transcript 2:28-2:53; the config line "index top k 512" at
+ * 2:00-2:13).  Results are exact: every value comes back bit-for-bit and no
+ * index repeats (DeepSeek V4.1 Flash, kernelbench model page, entry
+ * "Single-launch CUDA bitonic selection").
+ *
+ * Value order: -inf < negatives < -0.0 < +0.0 < positives < +inf.  NaN is
+ * not a value: a NaN inside a valid prefix is reported through the workspace
+ * status word (TOPK_STATUS_NAN) and is left out of the selection.
+ *
+ * Method: one threshold per row that only rises, a shared-memory candidate
+ * tray, 1024-element blocks streamed once in a seeded shuffled order, a
+ * bitonic sort that runs on the tray only, and for short batches a split of
+ * each row over several CTAs whose local winners a ticket-elected leader
+ * merges (video transcript 3:18-5:45).
+ *
+ * Memory: every pointer argument is caller-owned.  The library allocates no
+ * memory, frees none, keeps no device state between calls and never
+ * synchronises a stream except in topk_ws_status / topk_ws_stats, which say
+ * so.  All device work is enqueued on `stream` (a cudaStream_t; NULL means the
+ * legacy default stream) and runs on the device current at the call.
+ *
+ * Errors.  Return codes are decided on the host before anything is enqueued
+ * (a launch failure is the one exception, TOPK_ERR_LAUNCH).  Problems only the
+ * device can see (a NaN score, a length outside [0, n]) set bits in the
+ * workspace status word; the kernels never trap and always finish.
+ */
+#ifndef TOPK_SELECT_H
+#define TOPK_SELECT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define TOPK_OK 0
+#define TOPK_ERR_SHAPE 1  /* rows < 0, n < 1, n >= 2^31, row_stride < n,
+                             k < 1 or k > 2048, split out of range */
+#define TOPK_ERR_NULL 2   /* scores / out_vals / out_idx NULL with rows > 0 */
+#define TOPK_ERR_WS 3     /* ws NULL or not 256-byte aligned when needed */
+#define TOPK_ERR_LAUNCH 4 /* the CUDA launch reported an error */
+#define TOPK_ERR_ARG 5    /* another argument is invalid (see the function) */
+
+/* Status bits the device sets in the workspace status word (sticky until
+ * read by topk_ws_status). */
+#define TOPK_STATUS_NAN 1u        /* a NaN inside some row's valid prefix */
+#define TOPK_STATUS_BAD_LENGTH 2u /* lengths[r] outside [0, n]; clamped */
+#define TOPK_STATUS_TIMEOUT 4u    /* a bounded wait on a bulk copy gave up; the
+                                     affected rows' outputs are unspecified */
+
+/* Flags for topk_select_ex. */
+#define TOPK_FLAG_IDENTITY_ORDER 1u /* visit blocks in address order instead of
+                                       the shuffled order (diagnostic: the
+                                       result is the same, the speed is not) */
+
+/* Largest supported k. */
+#define TOPK_MAX_K 2048
+
+/*
+ * topk_ws_bytes -- workspace size, in bytes, that topk_select needs for this
+ * shape (with the automatic split plan).  Returns 0 for an invalid shape.
+ *
+ * The workspace holds a status word, per-row survivor and sort counters, the
+ * per-row tickets of the split-row leader election and, when rows are split,
+ * the CTAs' partial top-k lists (8 bytes x k rounded up to a power of two, per
+ * CTA).  It is a pure function of (rows, n, k).
+ */
+size_t topk_ws_bytes(int32_t rows, int64_t n, int32_t k);
+
+/*
+ * topk_select -- row-wise top-k.
+ *
+ *   scores           device fp32, element (r, i) at scores[r * row_stride + i],
+ *                    read for i < L_r only.  Rows whose start is not 16-byte
+ *                    aligned are read with plain loads instead of bulk copies.
+ *   rows             number of rows (>= 0; 0 enqueues nothing).
+ *   n                logical row width, 1 <= n < 2^31.
+ *   row_stride       elements between row starts, >= n.
+ *   lengths_or_null  device int32[rows]: L_r, the valid prefix of row r, in
+ *                    [0, n]; NULL means L_r = n for every row.  A length
+ *                    outside [0, n] is clamped and sets TOPK_STATUS_BAD_LENGTH.
+ *   k                1 <= k <= 2048.
+ *   out_vals         device fp32[rows * k]; row r's results at r * k + j.
+ *   out_idx          device int32[rows * k], same layout.  Slots
+ *                    j >= min(k, L_r) hold (-inf, -1).  Nothing outside
+ *                    [0, rows * k) is written.
+ *   ws               device workspace of at least topk_ws_bytes(rows, n, k)
+ *                    bytes, 256-byte aligned, zero-filled once by the caller
+ *                    after allocation.  Every call leaves the tickets at zero,
+ *                    so the same workspace serves any number of later calls
+ *                    in stream order; two calls that may overlap on the GPU
+ *                    must not share one.
+ *   stream           cudaStream_t to enqueue on (NULL: legacy default stream).
+ *
+ * All offsets are computed in 64-bit.  Returns TOPK_OK or an error code above;
+ * on an error nothing is enqueued (except after TOPK_ERR_LAUNCH).
+ */
+int topk_select(const float* scores, int32_t rows, int64_t n,
+                int64_t row_stride, const int32_t* lengths_or_null, int32_t k,
+                float* out_vals, int32_t* out_idx, void* ws, void* stream);
+
+/*
+ * topk_split_plan -- the number of CTAs the automatic plan gives each row
+ * (1 = unsplit).  A pure function of (rows, n); 0 for an invalid shape.
+ */
+int32_t topk_split_plan(int32_t rows, int64_t n);
+
+/*
+ * topk_ws_bytes_ex -- workspace size for an explicit split factor `split`
+ * (0 = the automatic plan, else 1 <= split <= 64).  0 for an invalid shape.
+ */
+size_t topk_ws_bytes_ex(int32_t rows, int64_t n, int32_t k, int32_t split);
+
+/*
+ * topk_select_ex -- topk_select with the knobs the tests and the benchmark
+ * use.  `split`: CTAs per row (0 = automatic, else 1..64; the workspace must
+ * then be sized by topk_ws_bytes_ex with the same split).  `seed`: the 64-bit
+ * Philox4x32-10 key of the block visiting order (topk_select uses a fixed
+ * default).  `flags`: TOPK_FLAG_*.  The result never depends on split, seed
+ * or flags; only the speed and the survivor counters do.
+ */
+int topk_select_ex(const float* scores, int32_t rows, int64_t n,
+                   int64_t row_stride, const int32_t* lengths_or_null,
+                   int32_t k, float* out_vals, int32_t* out_idx, void* ws,
+                   void* stream, int32_t split, uint64_t seed, uint32_t flags);
+
+/*
+ * topk_ws_status -- synchronises `stream`, then reads and clears the status
+ * word of `ws` (TOPK_STATUS_* bits) into *status_out.  Returns TOPK_OK,
+ * TOPK_ERR_WS for a NULL/misaligned ws, TOPK_ERR_ARG for a NULL status_out,
+ * or TOPK_ERR_LAUNCH if a CUDA call fails.
+ */
+int topk_ws_status(void* ws, uint32_t* status_out, void* stream);
+
+/*
+ * topk_ws_stats -- synchronises `stream`, then copies to host memory and
+ * clears the per-row counters of `ws` laid out for (rows, n, k, split):
+ * survivors_out[r] = scores of row r admitted to a tray (each element is
+ * tested once, so this is the number of elements that reached a sort), and
+ * sorts_out[r] = tray sorts run for row r.  Either output may be NULL.
+ * Counters accumulate over calls until read.  Return codes as topk_ws_status.
+ */
+int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
+                  uint32_t* survivors_out, uint32_t* sorts_out, void* stream);
+
+/*
+ * topk_visit_order -- diagnostic: writes to device int32 order_out[m] the
+ * order in which a CTA visits the m <= 1024 blocks of one permutation chunk,
+ * given the chunk's row, its first block index in the row and the seed: the
+ * blocks sorted by (Philox4x32-10(counter = (first_block + j, row, 0, 0),
+ * key = seed) word 0 with its low 10 bits cleared, j).  Enqueued on `stream`.
+ * Returns TOPK_ERR_ARG for m outside [1, 1024] or a NULL order_out.
+ */
+int topk_visit_order(int32_t m, int32_t row, int64_t first_block,
+                     uint64_t seed, int32_t* order_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPK_SELECT_H */

@@ -6,11 +6,12 @@ seeded workloads.  The binding is imported lazily so that the generators can
 be used on a machine without the built library.
 """
 
+import importlib
+
 __all__ = ["binding", "synth"]
 
 
 def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
+    if name in ("binding", "synth", "build"):
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)
