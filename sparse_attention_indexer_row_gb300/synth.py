@@ -66,13 +66,22 @@ def uniform_pool(rows=4, n=16384, k=512, seed=1) -> Workload:
                     {"dist": "Uniform[-1,1)", "seed": seed})
 
 
-def normal_varlen(rows=64, n=131072, k=512, seed=2, lo=256) -> Workload:
-    """i.i.d. Normal(0,1) rows with valid length L_r ~ UniformInt[lo, n]."""
+def normal_varlen(rows=64, n=131072, k=512, seed=2, lo=256, short_rows=2) -> Workload:
+    """i.i.d. Normal(0,1) rows with valid length L_r ~ UniformInt[lo, n].
+
+    A uniform draw over [256, 131072] almost never lands below k, so the first
+    ``short_rows`` rows draw L_r ~ UniformInt[lo, k - 1] instead: the batch
+    always holds rows that return every valid position.
+    """
     rng = np.random.default_rng(seed)
     x = _normal(rng, (rows, n))
     lengths = rng.integers(lo, n, size=rows, endpoint=True).astype(np.int32)
+    ns = min(short_rows, rows)
+    if ns and k - 1 >= lo:
+        lengths[:ns] = rng.integers(lo, k - 1, size=ns, endpoint=True)
     return Workload(f"normal_varlen_{rows}x{n}_k{k}", x, k, n, lengths,
-                    {"dist": "Normal(0,1)", "lengths": f"UniformInt[{lo},{n}]",
+                    {"dist": "Normal(0,1)",
+                     "lengths": f"UniformInt[{lo},{n}], first {ns} rows UniformInt[{lo},{k - 1}]",
                      "seed": seed})
 
 

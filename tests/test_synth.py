@@ -22,7 +22,7 @@ def test_varlen_lengths():
     w = synth.normal_varlen(rows=64, n=131072)
     assert w.lengths.dtype == np.int32
     assert w.lengths.min() >= 256 and w.lengths.max() <= 131072
-    assert np.any(w.lengths < 512) or True   # covered at full size by the GPU tests
+    assert np.sum(w.lengths < 512) >= 2      # rows that return every valid position
 
 
 def test_relu_mix_shape():
