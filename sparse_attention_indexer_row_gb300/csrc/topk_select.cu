@@ -10,11 +10,18 @@
 // 32-bit survivor mask 5:10-5:22; the split-row leader merge 5:33-5:45.)
 //
 // GB300 mapping:
-//  * Each CTA (256 threads) owns one segment of one row.  Blocks of 4 KB are
-//    moved HBM -> shared memory by cp.async.bulk into an 8-stage ring, each
-//    stage signalled by an mbarrier with an expected transaction count.  One
-//    thread issues the copies; the ring keeps 32 KB per CTA in flight and
-//    three CTAs share an SM, which covers HBM latency at full bandwidth.
+//  * Work is cut into pieces (a run of blocks of one row) and each CTA streams
+//    its pieces through a ring of shared-memory stages.  A producer warp moves
+//    blocks HBM -> shared memory with cp.async.bulk (each stage a few blocks,
+//    signalled by an mbarrier with an expected byte count) and never takes
+//    part in sorting, so loads keep streaming -- across piece boundaries too --
+//    while the consumer warps sort.  Consumers free a stage through a
+//    second mbarrier as soon as its scores are in registers.
+//  * Two plans.  Short batches of full-length rows: a persistent grid of one
+//    CTA per SM, each owning an equal share of the batch's blocks laid end to
+//    end, so every SM streams the same number of bytes; rows that straddle a
+//    share boundary are split.  Otherwise: one CTA per row, or per row segment
+//    when a short batch of variable-length rows needs more CTAs.
 //  * Every element becomes the 64-bit word (order key << 32) | ~index.  The
 //    order key is the usual monotone map of float bits, so word order is value
 //    order with ties broken towards the smaller index, and one 64-bit compare
@@ -22,15 +29,24 @@
 //    V4.1 Flash, kernelbench model page, entry "Single-launch CUDA bitonic
 //    selection"; the ~index half gives the smaller-index tie rule.)
 //  * The per-element test first runs as one float compare that can only let
-//    too much through (it passes NaN and values equal to the threshold's), so
-//    the exact word compare runs only in warps where some lane passed.
+//    too much through (it passes NaN and values equal to the threshold's); the
+//    exact word compare runs only for element slots some lane of the warp
+//    flagged (found with one warp OR-reduction).
 //  * Survivors are compacted with __ballot_sync masks and __popc prefixes; one
-//    shared-memory atomicAdd per warp reserves tray space.
-//  * When a row is split across CTAs, each CTA publishes its sorted local top-k
-//    to the workspace, fences, and takes a ticket; the CTA that draws the last
-//    ticket merges all lists and writes the row (the atomic-ticket last-CTA
-//    combine of DeepSeek V4.1 Flash, kernelbench model page, entry on the
-//    split-KV paged decode), then resets the ticket for the next call.
+//    shared-memory atomicAdd per warp and slot reserves tray space.
+//  * The tray is sorted in batches of max(512, k') words (k' = k rounded up to
+//    a power of two) by a bitonic network that applies up to three strides per
+//    barrier round, then merged into the kept list: the element-wise max of the kept list against the reversed
+//    batch is a bitonic sequence holding the best k' of both, and a bitonic
+//    merge sorts it.  Words still waiting are re-tested against the raised
+//    threshold before the next batch.
+//  * A split row's CTAs share the best threshold any of them has reached
+//    through a 64-bit atomicMax word per row.  Each publishes its sorted local
+//    top-k to the workspace, fences, and takes a ticket; the CTA that draws the
+//    last ticket merges all lists (a tree of parallel pairwise merges in its
+//    shared memory) and writes the row (the atomic-ticket last-CTA combine of
+//    DeepSeek V4.1 Flash, kernelbench model page, entry on the split-KV paged
+//    decode), then resets the ticket and threshold word for the next call.
 //  * No kernel ever traps or waits without a bound: bad lengths and NaNs set
 //    workspace status bits, and every mbarrier wait gives up after a fixed
 //    number of polls, setting a status bit.
@@ -40,37 +56,64 @@
 
 #include <atomic>
 
+#include "device_util.cuh"
 #include "topk_select.h"
 
+namespace topk {
 namespace {
 
-constexpr int kBlock = 1024;           // elements per block ("blocks of 1,024")
-constexpr int kThreads = 256;          // threads per CTA
-constexpr int kPerThread = kBlock / kThreads;  // 4 elements = one float4
-constexpr int kRing = 8;               // bulk-copy ring stages of one block
-constexpr int kFreshCap = 2048;        // tray room for new survivors
-constexpr int kSortTrigger = 1024;     // sort once more than this many wait
-constexpr int kPermChunk = 1024;       // blocks shuffled together
+constexpr int kBlock = 1024;          // elements per block ("blocks of 1,024")
+constexpr int kPermChunk = 1024;      // blocks shuffled together
+constexpr int kMinBatch = 512;        // tray sort batch (at least k')
 constexpr int kMaxSplit = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait gives up
 
-// Automatic split plan: enough CTAs for about two per SM of a 152-SM GB300,
-// segments of at least kMinSegBlocks blocks, at most kAutoMaxSplit per row.
-constexpr int kTargetCtas = 304;
-constexpr int kMinSegBlocks = 8;
-constexpr int kAutoMaxSplit = 16;
+// Launch plan, tuned for GB300's 152 SMs (results never depend on it).
+constexpr int kSms = 152;
+constexpr int kMaxFlatCtas = 256;     // persistent grid cap (workspace slots)
+constexpr int kMinFlatBlocks = 32;    // at least 128 KB per persistent CTA
+constexpr int kMinSegBlocks = 32;     // at least 128 KB per split segment
+constexpr int kManyRows = kSms;       // rows per call from which each gets a CTA
 
 constexpr uint64_t kDefaultSeed = 0x5EEDC0DE1234ABCDull;
 
+// CTA shapes: consumer warps, blocks per ring stage, ring stages, CTAs/SM.
+template <int NW_, int BPS_, int NSTAGE_, int MINB_>
+struct Shape {
+  static constexpr int NW = NW_;
+  static constexpr int BPS = BPS_;
+  static constexpr int NSTAGE = NSTAGE_;
+  static constexpr int MIN_BLOCKS = MINB_;
+  static constexpr int NC = NW * 32;               // consumer threads
+  static constexpr int NTHREADS = NC + 32;         // plus the producer warp
+  static constexpr int EPT = BPS * kBlock / NC;    // elements per thread per stage
+  static constexpr int F4 = EPT / 4;               // float4 loads per thread per stage
+  static constexpr int STAGE_FLOATS = BPS * kBlock;
+  static_assert(EPT % 4 == 0, "whole float4s per thread");
+  static_assert(EPT <= 32, "candidate bits fit one word");
+  static_assert(NC == 256 || NC == 512, "batch sorts are instantiated for 256 or 512 consumers");
+};
+
+using BigShape = Shape<16, 4, 8, 1>;    // 544 threads, 128 KB ring, 1 CTA/SM
+using SmallShape = Shape<8, 1, 8, 3>;   // 288 threads, 32 KB ring, 3 CTAs/SM
+
+// Plans.
+constexpr int kPlanRows = 0;   // CTA = (row, segment)
+constexpr int kPlanFlat = 1;   // CTA = equal share of the batch's blocks
+
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned):
-//   [0, 256)            header: u32 status
-//   tickets  u32[rows]  split-row leader election, zero between calls
-//   survivors u32[rows] elements admitted to a tray, per row (accumulating)
-//   sorts    u32[rows]  tray sorts per row (accumulating)
-//   partials u64[rows][split][kp]  when split > 1
+//   [0, 256)              header: u32 status
+//   tickets   u32[rows]   split-row leader election, zero between calls
+//   survivors u32[rows]   elements admitted to a tray, per row (accumulating)
+//   sorts     u32[rows]   tray sort batches per row (accumulating)
+//   theta     u64[rows]   split rows: best threshold word any of the row's CTAs
+//                         has reached, zero between calls
+//   partials  u64[slots][kp]  local top-k lists of split rows; slots =
+//                         max(rows * split, 2 * kMaxFlatCtas) when rows can
+//                         be split, else none
 struct WsLayout {
-  size_t tickets, survivors, sorts, partials, total;
+  size_t tickets, survivors, sorts, theta, partials, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -81,7 +124,33 @@ inline int next_pow2(int x) {
   return p;
 }
 
-WsLayout ws_layout(int32_t rows, int32_t kp, int32_t split) {
+bool shape_ok(int32_t rows, int64_t n, int32_t k) {
+  return rows >= 0 && n >= 1 && n <= INT32_MAX && k >= 1 && k <= TOPK_MAX_K;
+}
+
+int32_t auto_split(int32_t rows, int64_t n) {
+  if (rows <= 0 || rows >= kManyRows) return 1;
+  const int64_t m = (n + kBlock - 1) / kBlock;
+  int64_t s = kSms / rows;
+  const int64_t by_len = m / kMinSegBlocks;
+  if (s > by_len) s = by_len;
+  if (s > kMaxSplit) s = kMaxSplit;
+  if (s < 1) s = 1;
+  return int32_t(s);
+}
+
+// Partial-list slots a call may need.  With the automatic plan a short batch
+// may run either plan (the choice depends on whether lengths are passed).
+size_t partial_slots(int32_t rows, int32_t split_arg, int32_t split) {
+  size_t slots = split > 1 ? size_t(rows) * size_t(split) : 0;
+  if (split_arg == 0 && rows > 0 && rows < kManyRows) {
+    const size_t flat = 2 * size_t(kMaxFlatCtas);
+    if (flat > slots) slots = flat;
+  }
+  return slots;
+}
+
+WsLayout ws_layout(int32_t rows, int32_t kp, size_t slots) {
   WsLayout L;
   size_t off = 256;
   L.tickets = off;
@@ -90,185 +159,169 @@ WsLayout ws_layout(int32_t rows, int32_t kp, int32_t split) {
   off = align256(off + sizeof(uint32_t) * size_t(rows));
   L.sorts = off;
   off = align256(off + sizeof(uint32_t) * size_t(rows));
+  L.theta = off;
+  off = align256(off + sizeof(uint64_t) * size_t(rows));
   L.partials = off;
-  if (split > 1) off = align256(off + sizeof(uint64_t) * size_t(rows) * split * kp);
+  off = align256(off + sizeof(uint64_t) * slots * size_t(kp));
   L.total = off;
   return L;
 }
 
-bool shape_ok(int32_t rows, int64_t n, int32_t k) {
-  return rows >= 0 && n >= 1 && n <= INT32_MAX && k >= 1 && k <= TOPK_MAX_K;
-}
-
-int32_t auto_split(int32_t rows, int64_t n) {
-  const int64_t m = (n + kBlock - 1) / kBlock;
-  if (rows <= 0) return 1;
-  if (rows >= kTargetCtas) return 1;
-  int64_t s = (kTargetCtas + rows - 1) / rows;
-  s = s < m / kMinSegBlocks ? s : m / kMinSegBlocks;
-  if (s > kAutoMaxSplit) s = kAutoMaxSplit;
-  if (s < 1) s = 1;
-  return int32_t(s);
-}
-
 // ---------------------------------------------------------------------------
-// Device helpers.
+// Kernel parameters and shared-memory layout.
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+struct Params {
+  const float* scores;
+  int64_t row_stride;
+  int64_t n;
+  const int32_t* lengths;  // may be null
+  int32_t rows;
+  int32_t k;
+  int32_t kp;          // next power of two >= k: kept-list capacity
+  int32_t batch;       // tray sort batch: max(kMinBatch, kp)
+  int32_t plan;        // kPlanRows or kPlanFlat
+  int32_t split;       // kPlanRows: CTAs per row
+  int32_t seg_blocks;  // kPlanRows: blocks per segment
+  int32_t m_full;      // blocks per full row
+  float* out_vals;
+  int32_t* out_idx;
+  uint32_t* status;
+  uint32_t* tickets;
+  uint32_t* survivors;
+  uint32_t* sorts;
+  unsigned long long* row_theta;
+  uint64_t* partials;
+  uint32_t seed_lo, seed_hi;
+  uint32_t flags;
+};
+
+struct SmemLayout {
+  int ring, kept, fresh, perm, bars, total;
+};
+
+__host__ __device__ inline int batch_of(int kp) { return kp > kMinBatch ? kp : kMinBatch; }
+
+template <class S>
+__host__ __device__ inline SmemLayout smem_layout(int kp) {
+  const int batch = batch_of(kp);
+  SmemLayout L;
+  int off = 0;
+  L.ring = off;
+  off += S::NSTAGE * S::STAGE_FLOATS * int(sizeof(float));
+  L.kept = off;
+  off += kp * int(sizeof(uint64_t));
+  L.fresh = off;
+  off += (batch + S::STAGE_FLOATS) * int(sizeof(uint64_t));
+  L.perm = off;
+  off += 2 * kPermChunk * int(sizeof(uint32_t));
+  L.bars = off;
+  off += (2 * S::NSTAGE + 2) * int(sizeof(uint64_t));
+  L.total = off;
+  return L;
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
+struct CtaState {
+  int cnt;          // words waiting in the tray
+  int cnt2;         // scratch counter for re-filtering
+  int leader;       // this CTA drew the last ticket
+  int ragged[2];    // per visit-order buffer: position of the ragged block, or -1
+  uint64_t theta;   // the threshold word (0 = nothing kept yet)
+};
+
+// A piece: blocks [b_begin, b_end) of row r, processed with one tray.
+struct Piece {
+  int32_t r;
+  int32_t b_begin, b_end;
+  int32_t m;             // blocks in the row
+  uint32_t L;            // valid length of the row
+  int32_t contributors;  // CTAs sharing the row (1 = unsplit)
+  int32_t slot;          // partial slot when split
+  int32_t first_cta;     // kPlanFlat: first CTA of the row
+};
+
+// Cursor over a CTA's chunks (at most kPermChunk blocks of one piece).
+struct Cursor {
+  bool valid;
+  int32_t pi;       // piece index within the CTA
+  Piece pc;
+  int32_t cb;       // first block of the chunk (row-local)
+  int32_t cs;       // blocks in the chunk
+};
+
+__device__ __forceinline__ int64_t flat_lo(int64_t g, int64_t M, int64_t G) { return g * M / G; }
+__device__ __forceinline__ int32_t flat_cta_of(int64_t b, int64_t M, int64_t G) {
+  return int32_t(((b + 1) * G - 1) / M);
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: false if the phase did not complete within `limit` polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t it = 0; it < limit; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-// Bulk copy global -> this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 32x32
-// multiplies with the high halves xor-ed into the other words and the key.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int i = 0; i < 10; ++i) {
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+// The pi-th piece of this CTA, or false when there is none.
+__device__ bool get_piece(const Params& p, int32_t pi, Piece& out) {
+  const uint32_t cta = blockIdx.x;
+  if (p.plan == kPlanRows) {
+    if (pi != 0) return false;
+    const int32_t r = int32_t(cta / uint32_t(p.split));
+    const int32_t s = int32_t(cta % uint32_t(p.split));
+    int64_t L = p.lengths ? int64_t(p.lengths[r]) : p.n;
+    if (L < 0) L = 0;
+    if (L > p.n) L = p.n;
+    const int32_t m = int32_t((L + kBlock - 1) / kBlock);
+    const int32_t contributors = m == 0 ? 1 : (m + p.seg_blocks - 1) / p.seg_blocks;
+    if (s >= contributors) return false;
+    out.r = r;
+    out.m = m;
+    out.L = uint32_t(L);
+    out.b_begin = s * p.seg_blocks;
+    out.b_end = m == 0 ? 0 : min(m, out.b_begin + p.seg_blocks);
+    out.contributors = contributors;
+    out.slot = r * p.split + s;
+    out.first_cta = 0;
+    return true;
   }
-  return c;
+  const int64_t M = int64_t(p.rows) * p.m_full;
+  const int64_t G = gridDim.x;
+  const int64_t lo = flat_lo(cta, M, G), hi = flat_lo(cta + 1, M, G);
+  const int64_t r0 = lo / p.m_full;
+  const int64_t r = r0 + pi;
+  const int64_t rs = r * p.m_full;
+  if (r >= p.rows || rs >= hi) return false;
+  out.r = int32_t(r);
+  out.m = p.m_full;
+  out.L = uint32_t(p.n);
+  out.b_begin = int32_t(lo > rs ? lo - rs : 0);
+  out.b_end = int32_t(hi - rs < p.m_full ? hi - rs : p.m_full);
+  const int32_t g0 = flat_cta_of(rs, M, G), g1 = flat_cta_of(rs + p.m_full - 1, M, G);
+  out.contributors = g1 - g0 + 1;
+  out.first_cta = g0;
+  out.slot = 2 * int32_t(cta) + (r == r0 ? 0 : 1);
+  return true;
 }
 
-// Monotone map of float bits: unsigned order of the result = value order,
-// with -0.0 below +0.0.
-__device__ __forceinline__ uint32_t order_key(uint32_t bits) {
-  return bits ^ (uint32_t(int32_t(bits) >> 31) | 0x80000000u);
+__device__ void cursor_first(const Params& p, Cursor& c) {
+  c.pi = 0;
+  c.valid = get_piece(p, 0, c.pc);
+  c.cb = c.valid ? c.pc.b_begin : 0;
+  c.cs = c.valid ? min(c.pc.b_end - c.pc.b_begin, kPermChunk) : 0;
 }
 
-__device__ __forceinline__ float key_to_float(uint32_t key) {
-  const uint32_t bits = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
-  return __uint_as_float(bits);
-}
-
-// Smallest float whose key is >= the threshold word's key; -inf while the
-// threshold is still the empty word 0.
-__device__ __forceinline__ float threshold_float(uint64_t th) {
-  const uint32_t hi = uint32_t(th >> 32);
-  return hi < 0x007FFFFFu ? -__int_as_float(0x7F800000) : key_to_float(hi);
-}
-
-__device__ __forceinline__ int next_pow2_dev(int x) {
-  return x <= 1 ? 1 : 1 << (32 - __clz(x - 1));
-}
-
-// Bitonic sort, descending, of a power-of-two-sized shared array.  Ends with
-// a CTA barrier.
-__device__ void bitonic_sort_desc(uint64_t* a, int n) {
-  const int half = n >> 1;
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = threadIdx.x; t < half; t += kThreads) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const uint64_t x = a[i], y = a[j];
-        const bool desc = (i & size) == 0;
-        if ((x < y) == desc) {
-          a[i] = y;
-          a[j] = x;
-        }
-      }
-      __syncthreads();
-    }
+__device__ void cursor_next(const Params& p, Cursor& c) {
+  c.cb += c.cs;
+  if (c.cb >= c.pc.b_end) {
+    c.pi += 1;
+    c.valid = get_piece(p, c.pi, c.pc);
+    if (!c.valid) return;
+    c.cb = c.pc.b_begin;
   }
-}
-
-// Sorts a bitonic power-of-two-sized shared array descending.  Ends with a
-// CTA barrier.
-__device__ void bitonic_merge_desc(uint64_t* a, int n) {
-  const int half = n >> 1;
-  for (int stride = half; stride > 0; stride >>= 1) {
-    for (int t = threadIdx.x; t < half; t += kThreads) {
-      const int i = 2 * t - (t & (stride - 1));
-      const int j = i + stride;
-      const uint64_t x = a[i], y = a[j];
-      if (x < y) {
-        a[i] = y;
-        a[j] = x;
-      }
-    }
-    __syncthreads();
-  }
-}
-
-// Bitonic sort, ascending, of a power-of-two-sized shared u32 array.
-__device__ void bitonic_sort_asc_u32(uint32_t* a, int n) {
-  const int half = n >> 1;
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = threadIdx.x; t < half; t += kThreads) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const uint32_t x = a[i], y = a[j];
-        const bool asc = (i & size) == 0;
-        if ((x > y) == asc) {
-          a[i] = y;
-          a[j] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  c.cs = min(c.pc.b_end - c.cb, kPermChunk);
 }
 
 // Visiting order of `cs` consecutive blocks of row `row` starting at block
 // `first`: the blocks sorted by a Philox draw with the low 10 bits replaced by
 // the block's position, so the order is a permutation no matter the draws and
 // never depends on the scores.  perm[p] & 1023 = position visited p-th.
+template <class T>
 __device__ void build_visit_order(uint32_t* perm, int cs, int64_t first, int32_t row,
-                                  uint32_t seed_lo, uint32_t seed_hi, bool identity) {
+                                  uint32_t seed_lo, uint32_t seed_hi, bool identity, int t) {
   const int p2 = next_pow2_dev(cs);
-  for (int j = threadIdx.x; j < p2; j += kThreads) {
+  for (int j = t; j < p2; j += T::size) {
     uint32_t key = 0xFFFFFFFFu;
     if (j < cs) {
       if (identity) {
@@ -281,309 +334,35 @@ __device__ void build_visit_order(uint32_t* perm, int cs, int64_t first, int32_t
     }
     perm[j] = key;
   }
-  __syncthreads();
-  bitonic_sort_asc_u32(perm, p2);
+  T::sync();
+  bitonic_network<T, uint32_t, false>(perm, p2, 2, 1, 0, t);
 }
 
-
-// ---------------------------------------------------------------------------
-// The selection kernel.
-
-struct Params {
-  const float* scores;
-  int64_t row_stride;
-  int64_t n;
-  const int32_t* lengths;  // may be null
-  int32_t rows;
-  int32_t k;
-  int32_t kp;          // next power of two >= k: kept-list capacity
-  int32_t split;       // CTAs per row
-  int32_t seg_blocks;  // blocks per segment
-  float* out_vals;
-  int32_t* out_idx;
-  uint32_t* status;
-  uint32_t* tickets;
-  uint32_t* survivors;
-  uint32_t* sorts;
-  uint64_t* partials;
-  uint32_t seed_lo, seed_hi;
-  uint32_t flags;
-};
-
-struct SmemLayout {
-  // byte offsets into dynamic shared memory
-  int ring, kept, fresh, perm, bars, total;
-};
-
-__host__ __device__ inline SmemLayout smem_layout(int kp) {
-  SmemLayout L;
-  int off = 0;
-  L.ring = off;
-  off += kRing * kBlock * int(sizeof(float));
-  L.kept = off;
-  off += kp * int(sizeof(uint64_t));
-  L.fresh = off;
-  off += kFreshCap * int(sizeof(uint64_t));
-  L.perm = off;
-  off += kPermChunk * int(sizeof(uint32_t));
-  L.bars = off;
-  off += kRing * int(sizeof(uint64_t));
-  L.total = off;
-  return L;
-}
-
-struct CtaState {
-  int cnt;          // new words waiting in the tray
-  int leader;       // this CTA drew the last ticket
-  uint64_t theta;   // the threshold word (0 = nothing kept yet)
-};
-
-// Sort the waiting words, merge them with the kept list, keep the best kp
-// (the first k of which are the running answer) and raise the threshold to
-// the k-th kept word.  Called by all threads after a barrier; `pow2` is a
-// power of two >= max(cnt, kp) and <= kFreshCap.
-__device__ void tray_sort(uint64_t* kept, uint64_t* fresh, CtaState* st, int kp, int k,
-                          int pow2) {
-  const int cnt = st->cnt;
-  for (int t = cnt + threadIdx.x; t < pow2; t += kThreads) fresh[t] = 0ull;
-  __syncthreads();
-  bitonic_sort_desc(fresh, pow2);
-  // kept and fresh are both sorted descending: the element-wise max of kept[j]
-  // and fresh[kp-1-j] holds the best kp of their union as a bitonic sequence.
-  for (int j = threadIdx.x; j < kp; j += kThreads) {
-    const uint64_t a = kept[j], b = fresh[kp - 1 - j];
+// Merge the first kp words of a sorted-descending `batch` into the kept list:
+// the best kp of both end up sorted in kept.
+template <class T>
+__device__ void merge_into_kept(uint64_t* kept, const uint64_t* batch, int kp, int t) {
+  for (int j = t; j < kp; j += T::size) {
+    const uint64_t a = kept[j], b = batch[kp - 1 - j];
     kept[j] = a > b ? a : b;
   }
-  __syncthreads();
-  bitonic_merge_desc(kept, kp);
-  if (threadIdx.x == 0) {
-    st->theta = kept[k - 1];
-    st->cnt = 0;
-  }
-  __syncthreads();
+  T::sync();
+  bitonic_network<T, uint64_t, true>(kept, kp, kp, 1, 0, t);
 }
 
-__global__ void __launch_bounds__(kThreads)
-topk_select_kernel(const Params p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout sl = smem_layout(p.kp);
-  float* ring = reinterpret_cast<float*>(smem + sl.ring);
-  uint64_t* kept = reinterpret_cast<uint64_t*>(smem + sl.kept);
-  uint64_t* fresh = reinterpret_cast<uint64_t*>(smem + sl.fresh);
-  uint32_t* perm = reinterpret_cast<uint32_t*>(smem + sl.perm);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bars);
-  __shared__ CtaState st;
+// Sorts the first B tray words (descending, in place) and merges the first
+// kp of them into the kept list.  Entered right after a team barrier.
+template <class T>
+__device__ void sort_batch(int B, uint64_t* fresh, uint64_t* kept, int kp, int t) {
+  bitonic_network<T, uint64_t, true>(fresh, B, 2, 1, 0, t);
+  merge_into_kept<T>(kept, fresh, kp, t);
+}
 
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int32_t r = int32_t(blockIdx.x / uint32_t(p.split));
-  const int32_t s = int32_t(blockIdx.x % uint32_t(p.split));
-
-  // a1: the row's valid length and this CTA's segment.
-  int64_t L = p.lengths ? int64_t(p.lengths[r]) : p.n;
-  if (L < 0 || L > p.n) {
-    if (tid == 0 && s == 0) atomicOr(p.status, TOPK_STATUS_BAD_LENGTH);
-    L = L < 0 ? 0 : p.n;
-  }
-  const int32_t m = int32_t((L + kBlock - 1) / kBlock);
-  const int32_t contributors = m == 0 ? 1 : (m + p.seg_blocks - 1) / p.seg_blocks;
-  if (s >= contributors) return;  // this row is too short to reach segment s
-  const int32_t b0 = s * p.seg_blocks;
-  const int32_t nb = m == 0 ? 0 : min(m - b0, p.seg_blocks);
-
-  const float* row = p.scores + int64_t(r) * p.row_stride;
-  const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-  const bool identity = (p.flags & TOPK_FLAG_IDENTITY_ORDER) != 0;
-  const int kp = p.kp, k = p.k;
-
-  for (int j = tid; j < kp; j += kThreads) kept[j] = 0ull;
-  if (tid == 0) {
-    st.cnt = 0;
-    st.theta = 0ull;
-    st.leader = 0;
-    for (int i = 0; i < kRing; ++i) mbar_init(&bars[i], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-
-  uint64_t th = 0ull;
-  float thf = threshold_float(th);
-  uint32_t admitted = 0, nsorts = 0;
-  bool saw_nan = false, timed_out = false;
-  uint32_t g = 0;  // blocks consumed by this CTA so far (ring phase counter)
-
-  for (int32_t cb = 0; cb < nb; cb += kPermChunk) {
-    const int cs = min(nb - cb, kPermChunk);
-    const int64_t chunk_first = int64_t(b0) + cb;
-    // a2: the visiting order of this chunk (never reads the scores).
-    build_visit_order(perm, cs, chunk_first, r, p.seed_lo, p.seed_hi, identity);
-
-    // a3: producer prologue (one thread fills the ring).
-    auto issue = [&](int i, uint32_t stage) {
-      const int64_t blk = chunk_first + int64_t(perm[i] & 1023u);
-      const int64_t e0 = blk * kBlock;
-      const int valid = int(min(int64_t(kBlock), L - e0));
-      const uint32_t bytes = aligned ? uint32_t(valid & ~3) * 4u : 0u;
-      uint64_t* bar = &bars[stage];
-      if (bytes) {
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(ring + stage * kBlock, row + e0, bytes, bar);
-      } else {
-        mbar_arrive(bar);
-      }
-    };
-    if (tid == 0) {
-      fence_proxy_async_smem();
-      for (int i = 0; i < min(cs, kRing); ++i) issue(i, (g + i) % kRing);
-    }
-
-    for (int i = 0; i < cs; ++i, ++g) {
-      const uint32_t stage = g % kRing;
-      const uint32_t parity = (g / kRing) & 1u;
-      // After one wait has given up, later ones poll once: the CTA drains in
-      // bounded time and reports TOPK_STATUS_TIMEOUT.
-      if (!mbar_wait(&bars[stage], parity, timed_out ? 1u : kWaitLimit)) timed_out = true;
-
-      const int64_t blk = chunk_first + int64_t(perm[i] & 1023u);
-      const int64_t e0 = blk * kBlock;
-      const int valid = int(min(int64_t(kBlock), L - e0));
-      const int copied = aligned ? (valid & ~3) : 0;
-      const int j0 = tid * kPerThread;
-      const float* src = ring + stage * kBlock;
-
-      float x[kPerThread];
-      bool present[kPerThread];
-      if (j0 + kPerThread <= copied) {
-        const float4 v = *reinterpret_cast<const float4*>(src + j0);
-        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-#pragma unroll
-        for (int e = 0; e < kPerThread; ++e) present[e] = true;
-      } else {
-#pragma unroll
-        for (int e = 0; e < kPerThread; ++e) {
-          const int j = j0 + e;
-          present[e] = j < valid;
-          x[e] = 0.f;
-          if (j < copied) x[e] = src[j];
-          else if (j < valid) x[e] = __ldg(row + e0 + j);
-        }
-      }
-
-      // a4: one question per element.  The float compare passes a superset of
-      // the exact survivors (equal values, NaN); the word compare decides.
-      bool maybe[kPerThread];
-      bool any = false;
-      bool over = false;  // lane 0: this warp's add pushed the tray past the mark
-#pragma unroll
-      for (int e = 0; e < kPerThread; ++e) {
-        maybe[e] = present[e] && !(x[e] < thf);
-        any |= maybe[e];
-      }
-      if (__any_sync(0xFFFFFFFFu, any)) {
-        uint64_t w[kPerThread];
-        bool pass[kPerThread];
-#pragma unroll
-        for (int e = 0; e < kPerThread; ++e) {
-          const uint32_t bits = __float_as_uint(x[e]);
-          const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
-          saw_nan |= maybe[e] && nan;
-          const uint32_t idx = uint32_t(e0 + j0 + e);
-          w[e] = (uint64_t(order_key(bits)) << 32) | uint64_t(~idx);
-          pass[e] = maybe[e] && !nan && w[e] > th;
-        }
-        // a5: ballot masks and popc prefixes; one atomic per warp.
-        uint32_t mask[kPerThread];
-        int total = 0;
-#pragma unroll
-        for (int e = 0; e < kPerThread; ++e) {
-          mask[e] = __ballot_sync(0xFFFFFFFFu, pass[e]);
-          total += __popc(mask[e]);
-        }
-        if (total) {
-          int base = 0;
-          if (lane == 0) {
-            base = atomicAdd(&st.cnt, total);
-            over = base + total > kSortTrigger;
-          }
-          base = __shfl_sync(0xFFFFFFFFu, base, 0);
-          const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-          for (int e = 0; e < kPerThread; ++e) {
-            if (pass[e]) fresh[base + __popc(mask[e] & lt)] = w[e];
-            base += __popc(mask[e]);
-          }
-        }
-      }
-      // The stage is consumed.  The tray count only grows within a block, so
-      // it ends past the mark exactly when some warp's own add took it there;
-      // deciding through the barrier keeps every thread on the same path even
-      // though fast threads may start adding the next block's survivors.
-      const bool need_sort = __syncthreads_or(over) != 0;
-
-      if (tid == 0 && i + kRing < cs) {
-        fence_proxy_async_smem();
-        issue(i + kRing, stage);
-      }
-      // a6: tray sort once the high-water mark is passed.
-      if (need_sort) {
-        admitted += uint32_t(st.cnt);
-        ++nsorts;
-        tray_sort(kept, fresh, &st, kp, k, kFreshCap);
-        th = st.theta;
-        thf = threshold_float(th);
-      }
-    }
-  }
-
-  // Final sort of whatever still waits in the tray.
-  if (st.cnt > 0) {
-    admitted += uint32_t(st.cnt);
-    ++nsorts;
-    const int c = st.cnt;
-    tray_sort(kept, fresh, &st, kp, k, next_pow2_dev(max(c, kp)));
-  }
-  saw_nan = __syncthreads_or(saw_nan) != 0;
-  timed_out = __syncthreads_or(timed_out) != 0;
-  if (tid == 0) {
-    if (saw_nan) atomicOr(p.status, TOPK_STATUS_NAN);
-    if (timed_out) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
-    atomicAdd(&p.survivors[r], admitted);
-    atomicAdd(&p.sorts[r], nsorts);
-  }
-
-  // a7: split rows publish their list; the last ticket merges.
-  if (contributors > 1) {
-    uint64_t* mine = p.partials + (int64_t(r) * p.split + s) * kp;
-    for (int j = tid; j < kp; j += kThreads) mine[j] = kept[j];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      const uint32_t t = atomicAdd(&p.tickets[r], 1u);
-      st.leader = (t == uint32_t(contributors - 1));
-    }
-    __syncthreads();
-    if (!st.leader) return;
-    __threadfence();
-    for (int32_t o = 0; o < contributors; ++o) {
-      if (o == s) continue;
-      const uint64_t* other = p.partials + (int64_t(r) * p.split + o) * kp;
-      for (int j = tid; j < kp; j += kThreads) fresh[j] = __ldcg(other + j);
-      __syncthreads();
-      for (int j = tid; j < kp; j += kThreads) {
-        const uint64_t a = kept[j], b = fresh[kp - 1 - j];
-        kept[j] = a > b ? a : b;
-      }
-      __syncthreads();
-      bitonic_merge_desc(kept, kp);
-    }
-    if (tid == 0) atomicExch(&p.tickets[r], 0u);
-  }
-
-  // a8: unpack and write the row: value descending, (-inf, -1) padding.
-  float* ov = p.out_vals + int64_t(r) * k;
-  int32_t* oi = p.out_idx + int64_t(r) * k;
-  for (int j = tid; j < k; j += kThreads) {
+__device__ __forceinline__ void write_row(const Params& p, int32_t r, const uint64_t* kept, int t,
+                                          int nt) {
+  float* ov = p.out_vals + int64_t(r) * p.k;
+  int32_t* oi = p.out_idx + int64_t(r) * p.k;
+  for (int j = t; j < p.k; j += nt) {
     const uint64_t w = kept[j];
     if (w == 0ull) {
       ov[j] = -__int_as_float(0x7F800000);
@@ -595,29 +374,450 @@ topk_select_kernel(const Params p) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+// ---------------------------------------------------------------------------
+// The selection kernel.
+
+template <class S>
+__global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel(const Params p) {
+  using Cons = Team<S::NC, 1>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const SmemLayout sl = smem_layout<S>(p.kp);
+  float* ring = reinterpret_cast<float*>(smem + sl.ring);
+  uint64_t* kept = reinterpret_cast<uint64_t*>(smem + sl.kept);
+  uint64_t* fresh = reinterpret_cast<uint64_t*>(smem + sl.fresh);
+  uint32_t* perm = reinterpret_cast<uint32_t*>(smem + sl.perm);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sl.bars);
+  uint64_t* empty = full + S::NSTAGE;
+  uint64_t* perm_ready = empty + S::NSTAGE;
+  __shared__ CtaState st;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const bool identity = (p.flags & TOPK_FLAG_IDENTITY_ORDER) != 0;
+  const int kp = p.kp, k = p.k, B = p.batch;
+
+  // a1: lengths outside [0, n] are clamped and reported once per row.
+  if (p.plan == kPlanRows && p.lengths && tid == 0 && blockIdx.x % uint32_t(p.split) == 0) {
+    const int32_t L = p.lengths[blockIdx.x / uint32_t(p.split)];
+    if (L < 0 || int64_t(L) > p.n) atomicOr(p.status, TOPK_STATUS_BAD_LENGTH);
+  }
+
+  Cursor first;
+  cursor_first(p, first);
+  if (!first.valid) return;  // nothing for this CTA (a short row's spare segment)
+  if (first.pc.m == 0) {     // a row of length 0: all padding
+    for (int j = tid; j < kp; j += S::NTHREADS) kept[j] = 0ull;
+    __syncthreads();
+    write_row(p, first.pc.r, kept, tid, S::NTHREADS);
+    return;
+  }
+
+  for (int j = tid; j < kp; j += S::NTHREADS) kept[j] = 0ull;
+  if (tid == 0) {
+    st.cnt = 0;
+    st.cnt2 = 0;
+    st.theta = 0ull;
+    st.leader = 0;
+    st.ragged[0] = st.ragged[1] = -1;
+    for (int i = 0; i < S::NSTAGE; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], S::NW);
+    }
+    mbar_init(&perm_ready[0], 1);
+    mbar_init(&perm_ready[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  // ---------------- producer warp: a3, the bulk-copy stream ----------------
+  if (warp == S::NW) {
+    if (lane != 0) return;
+    bool gave_up = false;
+    uint32_t g = 0;
+    Cursor cur = first;
+    for (int c = 0; cur.valid; ++c, cursor_next(p, cur)) {
+      const uint32_t* pc = perm + (c & 1) * kPermChunk;
+      const float* row = p.scores + int64_t(cur.pc.r) * p.row_stride;
+      const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+      if (!mbar_wait(&perm_ready[c & 1], (c >> 1) & 1, gave_up ? 1u : kWaitLimit)) gave_up = true;
+      for (int i = 0; i < cur.cs; i += S::BPS, ++g) {
+        const uint32_t stage = g % S::NSTAGE;
+        if (g >= uint32_t(S::NSTAGE) &&
+            !mbar_wait(&empty[stage], ((g / S::NSTAGE) - 1) & 1, gave_up ? 1u : kWaitLimit))
+          gave_up = true;
+        uint32_t bytes[S::BPS];
+        const float* src[S::BPS];
+        uint32_t total = 0;
+#pragma unroll
+        for (int b = 0; b < S::BPS; ++b) {
+          bytes[b] = 0;
+          src[b] = row;
+          if (i + b < cur.cs && aligned) {
+            const uint32_t e0 = uint32_t(cur.cb + int32_t(pc[i + b] & 1023u)) * kBlock;
+            const uint32_t valid = min(uint32_t(kBlock), cur.pc.L - e0);
+            bytes[b] = (valid & ~3u) * 4u;
+            src[b] = row + e0;
+          }
+          total += bytes[b];
+        }
+        fence_proxy_async_smem();
+        if (total) {
+          mbar_arrive_expect_tx(&full[stage], total);
+#pragma unroll
+          for (int b = 0; b < S::BPS; ++b)
+            if (bytes[b])
+              bulk_load(ring + stage * S::STAGE_FLOATS + b * kBlock, src[b], bytes[b],
+                        &full[stage]);
+        } else {
+          mbar_arrive(&full[stage]);
+        }
+      }
+    }
+    if (gave_up) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  const int ct = tid;  // 0 .. NC-1
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint64_t th = 0ull;
+  float thf = threshold_float(th);
+  uint32_t admitted = 0, nsorts = 0;
+  bool saw_nan = false, timed_out = false;
+  uint32_t g = 0;
+  bool shared_theta = false;
+  int32_t row_r = 0;
+
+  // a2: the visiting order of a chunk, and where the row's ragged last block
+  // (if any) falls in it.
+  auto build_order = [&](const Cursor& cu, int buf) {
+    uint32_t* pb = perm + buf * kPermChunk;
+    build_visit_order<Cons>(pb, cu.cs, cu.cb, cu.pc.r, p.seed_lo, p.seed_hi, identity, ct);
+    const int32_t ragged_blk = (cu.pc.L & (kBlock - 1)) ? cu.pc.m - 1 : -1;
+    if (ct == 0) st.ragged[buf] = -1;
+    Cons::sync();
+    if (ragged_blk >= cu.cb && ragged_blk < cu.cb + cu.cs) {
+      for (int j = ct; j < cu.cs; j += S::NC)
+        if (int32_t(pb[j] & 1023u) == ragged_blk - cu.cb) st.ragged[buf] = j;
+    }
+    Cons::sync();
+    if (ct == 0) mbar_arrive(&perm_ready[buf]);
+  };
+
+  // a6: sort batches of B tray words into the kept list until fewer than B
+  // wait, raising the threshold and re-testing the waiting words after each.
+  auto sort_batches = [&]() {
+    for (;;) {
+      const int cnt = st.cnt;
+      if (cnt < B) break;
+      ++nsorts;
+      sort_batch<Cons>(B, fresh, kept, kp, ct);
+      uint64_t nth = kept[k - 1];
+      const uint64_t cur = st.theta;
+      nth = nth > cur ? nth : cur;
+      uint64_t w[S::EPT];
+      bool keep[S::EPT];
+#pragma unroll
+      for (int u = 0; u < S::EPT; ++u) {
+        const int t = B + ct + u * S::NC;
+        w[u] = t < cnt ? fresh[t] : 0ull;
+        keep[u] = w[u] > nth;
+      }
+      Cons::sync();  // every waiting word is in registers
+#pragma unroll
+      for (int u = 0; u < S::EPT; ++u) {
+        const uint32_t mask = __ballot_sync(0xFFFFFFFFu, keep[u]);
+        if (mask) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&st.cnt2, __popc(mask));
+          base = __shfl_sync(0xFFFFFFFFu, base, 0);
+          if (keep[u]) fresh[base + __popc(mask & lt_mask)] = w[u];
+        }
+      }
+      if (ct == 0 && shared_theta) {
+        // share the raised threshold with the row's other CTAs
+        const unsigned long long old = atomicMax(&p.row_theta[row_r], (unsigned long long)nth);
+        if (old > nth) nth = old;
+      }
+      Cons::sync();
+      if (ct == 0) {
+        st.cnt = st.cnt2;
+        st.cnt2 = 0;
+        st.theta = nth;
+      }
+      Cons::sync();
+    }
+  };
+
+  // End of a piece: final sort, then the row's output (directly, or through
+  // the split-row ticket), then a clean tray for the next piece.
+  auto finish_piece = [&](const Piece& pc) {
+    const int cnt = st.cnt;
+    if (cnt > 0) {
+      ++nsorts;
+      for (int t = cnt + ct; t < B; t += S::NC) fresh[t] = 0ull;
+      Cons::sync();
+      sort_batch<Cons>(B, fresh, kept, kp, ct);
+    }
+    if (lane == 0 && admitted) atomicAdd(&p.survivors[pc.r], admitted);
+    admitted = 0;
+    if (ct == 0) atomicAdd(&p.sorts[pc.r], nsorts);
+    nsorts = 0;
+
+    if (pc.contributors == 1) {
+      write_row(p, pc.r, kept, ct, S::NC);
+    } else {
+      // a7: publish the local list, take a ticket; the last ticket merges.
+      uint64_t* mine = p.partials + int64_t(pc.slot) * kp;
+      for (int j = ct; j < kp; j += S::NC) mine[j] = kept[j];
+      __threadfence();
+      Cons::sync();
+      if (ct == 0) {
+        const uint32_t t = atomicAdd(&p.tickets[pc.r], 1u);
+        st.leader = (t == uint32_t(pc.contributors - 1));
+      }
+      Cons::sync();
+      if (st.leader) {
+        __threadfence();
+        // Gather lists into the idle tray and merge them as a tree of
+        // parallel pairwise merges; the running result stays in slot 0.
+        uint64_t* slots = fresh;
+        const int cap = (B + S::STAGE_FLOATS) / kp;
+        for (int j = ct; j < kp; j += S::NC) slots[j] = kept[j];
+        int next_other = 0;  // next contributor to gather (never this CTA)
+        const int self = p.plan == kPlanRows ? int(blockIdx.x % uint32_t(p.split))
+                                             : int(blockIdx.x) - pc.first_cta;
+        int remaining = pc.contributors - 1;
+        while (remaining > 0) {
+          const int take = min(remaining, cap - 1);
+          int o = next_other;
+          for (int q = 1; q <= take; ++q, ++o) {
+            if (o == self) ++o;
+            int64_t slot;
+            if (p.plan == kPlanRows) {
+              slot = int64_t(pc.r) * p.split + o;
+            } else {
+              const int64_t M = int64_t(p.rows) * p.m_full, G = gridDim.x;
+              const int64_t go = pc.first_cta + o;
+              slot = 2 * go + (flat_lo(go, M, G) / p.m_full == pc.r ? 0 : 1);
+            }
+            const uint64_t* other = p.partials + slot * kp;
+            for (int j = ct; j < kp; j += S::NC) slots[q * kp + j] = __ldcg(other + j);
+          }
+          next_other = o;
+          remaining -= take;
+          Cons::sync();
+          const int nl = take + 1;
+          for (int gap = 1; gap < nl; gap <<= 1) {
+            // pairs (q, q + gap) for q a multiple of 2*gap with q + gap < nl
+            const int npairs = (nl - gap + 2 * gap - 1) / (2 * gap);
+            for (int u = ct; u < npairs * kp; u += S::NC) {
+              const int pr = u / kp, j = u - pr * kp;
+              uint64_t* a = slots + (2 * gap * pr) * kp;
+              const uint64_t* b = a + gap * kp;
+              const uint64_t x = a[j], y = b[kp - 1 - j];
+              a[j] = x > y ? x : y;
+            }
+            Cons::sync();
+            bitonic_network<Cons, uint64_t, true>(slots, kp, kp, npairs, 2 * gap * kp, ct);
+          }
+        }
+        write_row(p, pc.r, slots, ct, S::NC);
+        if (ct == 0) {
+          p.row_theta[pc.r] = 0ull;
+          atomicExch(&p.tickets[pc.r], 0u);
+        }
+      }
+    }
+    // a clean tray for the next piece
+    Cons::sync();
+    for (int j = ct; j < kp; j += S::NC) kept[j] = 0ull;
+    if (ct == 0) {
+      st.cnt = 0;
+      st.theta = 0ull;
+      st.leader = 0;
+    }
+    Cons::sync();
+    th = 0ull;
+    thf = threshold_float(th);
+  };
+
+  Cursor cur = first;
+  build_order(cur, 0);
+  for (int c = 0; cur.valid; ++c) {
+    Cursor nxt = cur;
+    cursor_next(p, nxt);
+    // one chunk ahead, so the producer never waits long
+    if (nxt.valid) build_order(nxt, (c + 1) & 1);
+    const uint32_t* pc = perm + (c & 1) * kPermChunk;
+    const int ragged_pos = st.ragged[c & 1];
+    const float* row = p.scores + int64_t(cur.pc.r) * p.row_stride;
+    const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    const uint32_t L32 = cur.pc.L;
+    const int cs = cur.cs;
+    row_r = cur.pc.r;
+    shared_theta = cur.pc.contributors > 1;
+
+    for (int i = 0; i < cs; i += S::BPS, ++g) {
+      const uint32_t stage = g % S::NSTAGE;
+      if (!mbar_wait(&full[stage], (g / S::NSTAGE) & 1, timed_out ? 1u : kWaitLimit))
+        timed_out = true;
+      const float* src = ring + stage * S::STAGE_FLOATS;
+      // A clean stage holds BPS full blocks that were bulk-copied.
+      const bool clean = aligned && i + S::BPS <= cs &&
+                         (ragged_pos < i || ragged_pos >= i + S::BPS);
+
+      float x[S::EPT];
+      uint32_t cand = 0;  // bit e: element e may beat the threshold
+      if (clean) {
+#pragma unroll
+        for (int u = 0; u < S::F4; ++u) {
+          const float4 v = reinterpret_cast<const float4*>(src)[ct + S::NC * u];
+          x[4 * u + 0] = v.x;
+          x[4 * u + 1] = v.y;
+          x[4 * u + 2] = v.z;
+          x[4 * u + 3] = v.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        // a4: one question per element.  The float compare passes a superset
+        // of the exact survivors (equal values, NaN); the word compare decides.
+#pragma unroll
+        for (int e = 0; e < S::EPT; ++e) cand |= uint32_t(!(x[e] < thf)) << e;
+      } else {
+#pragma unroll
+        for (int u = 0; u < S::F4; ++u) {
+          const int q = ct + S::NC * u;
+          const int b = q >> 8;
+          const int j0 = (q & 255) * 4;
+          const int pos = i + b;
+          uint32_t valid = 0, copied = 0, e0 = 0;
+          if (pos < cs) {
+            e0 = uint32_t(cur.cb + int32_t(pc[pos] & 1023u)) * kBlock;
+            valid = min(uint32_t(kBlock), L32 - e0);
+            copied = aligned ? (valid & ~3u) : 0u;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t j = uint32_t(j0 + e);
+            float v = 0.f;
+            if (j < copied) v = src[b * kBlock + j];
+            else if (j < valid) v = __ldg(row + e0 + j);
+            x[4 * u + e] = v;
+            if (j < valid) cand |= uint32_t(!(v < thf)) << (4 * u + e);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+      }
+
+      bool over = false;
+      const uint32_t wcand = __reduce_or_sync(0xFFFFFFFFu, cand);
+      if (wcand) {
+        // a5: for each element slot some lane flagged, the exact word test, a
+        // ballot mask, __popc prefixes and one tray atomic per warp.
+#pragma unroll
+        for (int e = 0; e < S::EPT; ++e) {
+          if ((wcand >> e) & 1u) {
+            const bool mine = (cand >> e) & 1u;
+            bool pass = false;
+            uint64_t w = 0ull;
+            if (mine) {
+              const uint32_t bits = __float_as_uint(x[e]);
+              const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+              saw_nan |= nan;
+              const int q = ct + S::NC * (e >> 2);
+              const uint32_t blk = uint32_t(cur.cb + int32_t(pc[i + (q >> 8)] & 1023u));
+              const uint32_t idx = blk * kBlock + uint32_t((q & 255) * 4 + (e & 3));
+              w = (uint64_t(order_key(bits)) << 32) | uint64_t(~idx);
+              pass = !nan && w > th;
+            }
+            const uint32_t pm = __ballot_sync(0xFFFFFFFFu, pass);
+            if (pm) {
+              const int n_pass = __popc(pm);
+              int base = 0;
+              if (lane == 0) {
+                base = atomicAdd(&st.cnt, n_pass);
+                over |= base + n_pass >= B;
+                admitted += uint32_t(n_pass);
+              }
+              base = __shfl_sync(0xFFFFFFFFu, base, 0);
+              if (pass) fresh[base + __popc(pm & lt_mask)] = w;
+            }
+          }
+        }
+      }
+      // Pick up a threshold raised by the row's other CTAs now and then.
+      if (shared_theta && ct == 0 && (g & 7u) == 7u) {
+        const unsigned long long gt =
+            *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[row_r]);
+        if (gt > st.theta) st.theta = gt;
+      }
+      // The tray count only grows within a stage, so it ends at or past the
+      // batch size exactly when some warp's own add took it there; deciding
+      // through the barrier keeps every consumer on the same path.
+      if (Cons::sync_or(over)) sort_batches();
+      const uint64_t nt = st.theta;
+      if (nt != th) {
+        th = nt;
+        thf = threshold_float(th);
+      }
+    }
+    if (!nxt.valid || nxt.pi != cur.pi) finish_piece(cur.pc);
+    cur = nxt;
+  }
+
+  saw_nan = Cons::sync_or(saw_nan);
+  timed_out = Cons::sync_or(timed_out);
+  if (ct == 0) {
+    if (saw_nan) atomicOr(p.status, TOPK_STATUS_NAN);
+    if (timed_out) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
+  }
+}
+
+__global__ void __launch_bounds__(256)
 visit_order_kernel(int32_t m, int32_t row, int64_t first, uint32_t seed_lo, uint32_t seed_hi,
                    int32_t* out) {
   __shared__ uint32_t perm[kPermChunk];
-  build_visit_order(perm, m, first, row, seed_lo, seed_hi, false);
-  for (int j = threadIdx.x; j < m; j += kThreads) out[j] = int32_t(perm[j] & 1023u);
+  build_visit_order<Team<256, 0>>(perm, m, first, row, seed_lo, seed_hi, false, threadIdx.x);
+  for (int j = threadIdx.x; j < m; j += 256) out[j] = int32_t(perm[j] & 1023u);
 }
 
 // ---------------------------------------------------------------------------
 // Host side.
 
-std::atomic<uint64_t> g_configured_devices{0};
+struct DeviceInfo {
+  std::atomic<int> configured{0};
+  int sms = 0;
+};
+DeviceInfo g_devices[64];
 
-cudaError_t configure_device() {
+cudaError_t configure_device(int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-  if (bit && (g_configured_devices.load() & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem_layout(TOPK_MAX_K).total);
+  DeviceInfo* info = dev < 64 ? &g_devices[dev] : nullptr;
+  if (info && info->configured.load()) {
+    *sms = info->sms;
+    return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(topk_select_kernel<BigShape>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem_layout<BigShape>(TOPK_MAX_K).total);
   if (e != cudaSuccess) return e;
-  if (bit) g_configured_devices.fetch_or(bit);
+  e = cudaFuncSetAttribute(topk_select_kernel<SmallShape>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem_layout<SmallShape>(TOPK_MAX_K).total);
+  if (e != cudaSuccess) return e;
+  int count = 0;
+  e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  *sms = count;
+  if (info) {
+    info->sms = count;
+    info->configured.store(1);
+  }
   return cudaSuccess;
 }
 
@@ -626,6 +826,9 @@ int32_t resolve_split(int32_t rows, int64_t n, int32_t split) {
 }
 
 }  // namespace
+}  // namespace topk
+
+using namespace topk;
 
 extern "C" {
 
@@ -637,7 +840,7 @@ int32_t topk_split_plan(int32_t rows, int64_t n) {
 size_t topk_ws_bytes_ex(int32_t rows, int64_t n, int32_t k, int32_t split) {
   if (!shape_ok(rows, n, k) || split < 0 || split > kMaxSplit) return 0;
   const int32_t S = resolve_split(rows, n, split);
-  return ws_layout(rows, next_pow2(k), S).total;
+  return ws_layout(rows, next_pow2(k), partial_slots(rows, split, S)).total;
 }
 
 size_t topk_ws_bytes(int32_t rows, int64_t n, int32_t k) {
@@ -655,13 +858,11 @@ int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_str
 
   const int32_t S = resolve_split(rows, n, split);
   const int32_t kp = next_pow2(k);
-  const WsLayout wl = ws_layout(rows, kp, S);
+  const WsLayout wl = ws_layout(rows, kp, partial_slots(rows, split, S));
   const int64_t m_full = (n + kBlock - 1) / kBlock;
-  const int32_t seg = int32_t((m_full + S - 1) / S);
-  const int64_t grid = int64_t(rows) * S;
-  if (grid > INT32_MAX) return TOPK_ERR_SHAPE;
 
-  if (configure_device() != cudaSuccess) return TOPK_ERR_LAUNCH;
+  int sms = kSms;
+  if (configure_device(&sms) != cudaSuccess) return TOPK_ERR_LAUNCH;
 
   unsigned char* w = static_cast<unsigned char*>(ws);
   Params p;
@@ -672,21 +873,47 @@ int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_str
   p.rows = rows;
   p.k = k;
   p.kp = kp;
+  p.batch = batch_of(kp);
   p.split = S;
-  p.seg_blocks = seg;
+  p.seg_blocks = int32_t((m_full + S - 1) / S);
+  p.m_full = int32_t(m_full);
   p.out_vals = out_vals;
   p.out_idx = out_idx;
   p.status = reinterpret_cast<uint32_t*>(w);
   p.tickets = reinterpret_cast<uint32_t*>(w + wl.tickets);
   p.survivors = reinterpret_cast<uint32_t*>(w + wl.survivors);
   p.sorts = reinterpret_cast<uint32_t*>(w + wl.sorts);
+  p.row_theta = reinterpret_cast<unsigned long long*>(w + wl.theta);
   p.partials = reinterpret_cast<uint64_t*>(w + wl.partials);
   p.seed_lo = uint32_t(seed);
   p.seed_hi = uint32_t(seed >> 32);
   p.flags = flags;
 
-  const int smem = smem_layout(kp).total;
-  topk_select_kernel<<<unsigned(grid), kThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool flat = split == 0 && lengths_or_null == nullptr && rows < kManyRows;
+  if (flat) {
+    // persistent: one CTA per SM, equal shares of the batch's blocks
+    const int64_t M = int64_t(rows) * m_full;
+    int64_t G = sms < kMaxFlatCtas ? sms : kMaxFlatCtas;
+    const int64_t by_len = (M + kMinFlatBlocks - 1) / kMinFlatBlocks;
+    if (G > by_len) G = by_len;
+    if (G < 1) G = 1;
+    p.plan = kPlanFlat;
+    p.split = 1;
+    topk_select_kernel<BigShape><<<unsigned(G), BigShape::NTHREADS,
+                                   smem_layout<BigShape>(kp).total, st>>>(p);
+  } else {
+    const int64_t grid = int64_t(rows) * S;
+    if (grid > INT32_MAX) return TOPK_ERR_SHAPE;
+    p.plan = kPlanRows;
+    if (S == 1 && rows >= kManyRows) {
+      topk_select_kernel<SmallShape><<<unsigned(grid), SmallShape::NTHREADS,
+                                       smem_layout<SmallShape>(kp).total, st>>>(p);
+    } else {
+      topk_select_kernel<BigShape><<<unsigned(grid), BigShape::NTHREADS,
+                                     smem_layout<BigShape>(kp).total, st>>>(p);
+    }
+  }
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
 }
 
@@ -712,7 +939,8 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
                   uint32_t* survivors_out, uint32_t* sorts_out, void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TOPK_ERR_WS;
   if (!shape_ok(rows, n, k) || split < 0 || split > kMaxSplit) return TOPK_ERR_SHAPE;
-  const WsLayout wl = ws_layout(rows, next_pow2(k), resolve_split(rows, n, split));
+  const int32_t S = resolve_split(rows, n, split);
+  const WsLayout wl = ws_layout(rows, next_pow2(k), partial_slots(rows, split, S));
   unsigned char* w = static_cast<unsigned char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return TOPK_ERR_LAUNCH;
@@ -731,7 +959,7 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
 int topk_visit_order(int32_t m, int32_t row, int64_t first_block, uint64_t seed,
                      int32_t* order_out, void* stream) {
   if (m < 1 || m > kPermChunk || !order_out || first_block < 0) return TOPK_ERR_ARG;
-  visit_order_kernel<<<1, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  visit_order_kernel<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       m, row, first_block, uint32_t(seed), uint32_t(seed >> 32), order_out);
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
 }

@@ -116,6 +116,21 @@ def test_misaligned_and_padded_rows(stride_pad):
     assert_bit_exact(gv, gi, ov, oi, f"stride pad {stride_pad}")
 
 
+def test_multi_chunk_segments():
+    """Segments longer than one 1024-block shuffle chunk, in both CTA shapes."""
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((2, 2_500_003)).astype(np.float32)
+    gv, gi = run_gpu(x, 512, split=1)                 # few rows: the wide CTA
+    ov, oi = oracle_rows(x, 512)
+    assert_bit_exact(gv, gi, ov, oi, "2 x 2.5M unsplit")
+    y = rng.standard_normal((160, 1_100_005)).astype(np.float32)
+    lengths = rng.integers(0, 1_100_006, size=160).astype(np.int32)
+    lengths[:4] = [1_100_005, 1_048_577, 1_048_576, 0]
+    gv, gi = run_gpu(y, 1000, lengths=lengths)        # many rows: the narrow CTA
+    ov, oi = oracle_rows(y, 1000, lengths=lengths)
+    assert_bit_exact(gv, gi, ov, oi, "160 x 1.1M")
+
+
 def test_rows_zero_is_noop():
     from sparse_attention_indexer_row_gb300 import binding as B
     assert B.topk_select(0, 0, 100, 100, None, 5, 0, 0, 0) == 0
