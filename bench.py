@@ -138,9 +138,9 @@ class ClockSampler:
 
 def run_gb300(args, world, rank, local):
     import torch
-    import torch.distributed as dist
 
     from sparse_attention_indexer_row_gb300 import binding as B
+    from sparse_attention_indexer_row_gb300 import dist as D
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -162,9 +162,7 @@ def run_gb300(args, world, rank, local):
         if rc != 0:
             raise RuntimeError(f"topk_select returned {rc}")
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
+    barrier = D.barrier
 
     for i in range(args.warmup):
         step(i)
@@ -186,12 +184,8 @@ def run_gb300(args, world, rank, local):
         t1.record(stream)
         torch.cuda.synchronize()
         barrier()
-    total_ms = t0.elapsed_time(t1)
+    total_ms = D.max_over_ranks(t0.elapsed_time(t1), device=dev)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = world * rows / (ms_per_step / 1e3)
 
@@ -223,11 +217,7 @@ def run_gb300(args, world, rank, local):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = D.max_over_ranks(e0.elapsed_time(e1), device=dev)
     e2e_value = world * rows / (e2e_ms / args.steps / 1e3)
     h2d = host.numel() * 4 + (0 if w.lengths is None else rows * 4)
     d2h = rows * k * 8
@@ -235,7 +225,7 @@ def run_gb300(args, world, rank, local):
     # Survivor counters for one call (elements that reached a tray sort).
     B.topk_ws_stats(ws, rows, n, k, 0, stream)
     step(0)
-    rc, surv, sorts = B.topk_ws_stats(ws, rows, n, k, 0, stream)
+    rc, surv, sorts, adm = B.topk_ws_stats(ws, rows, n, k, 0, stream)
     rc2, status = B.topk_ws_status(ws, stream)
 
     if rank != 0:
@@ -313,6 +303,7 @@ def run_gb300(args, world, rank, local):
         "survivors": {
             "mean_per_row": round(float(np.mean(surv)), 1), "max_per_row": int(max(surv)),
             "sorts_per_row_mean": round(float(np.mean(sorts)), 2),
+            "admitted_per_row_mean": round(float(np.mean(adm)), 1),
             "bound_unsplit_row": round(1.5 * T * harmonic, 1),
             "split_per_row": split,
         },

@@ -146,13 +146,19 @@ int topk_ws_status(void* ws, uint32_t* status_out, void* stream);
 /*
  * topk_ws_stats -- synchronises `stream`, then copies to host memory and
  * clears the per-row counters of `ws` laid out for (rows, n, k, split):
- * survivors_out[r] = scores of row r admitted to a tray (each element is
- * tested once, so this is the number of elements that reached a sort), and
- * sorts_out[r] = tray sorts run for row r.  Either output may be NULL.
- * Counters accumulate over calls until read.  Return codes as topk_ws_status.
+ *   survivors_out[r]  words of row r that entered a bitonic tray sort -- the
+ *                     elements that ever reached a sorting step;
+ *   sorts_out[r]      bitonic tray sorts run for row r;
+ *   admitted_out[r]   elements of row r that passed the threshold test and
+ *                     went to the tray (a superset of the sorted ones: before
+ *                     each sort, words that can no longer reach the best k are
+ *                     dropped).
+ * Any output may be NULL.  Counters accumulate over calls until read.
+ * Return codes as topk_ws_status.
  */
 int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
-                  uint32_t* survivors_out, uint32_t* sorts_out, void* stream);
+                  uint32_t* survivors_out, uint32_t* sorts_out, uint32_t* admitted_out,
+                  void* stream);
 
 /*
  * topk_visit_order -- diagnostic: writes to device int32 order_out[m] the

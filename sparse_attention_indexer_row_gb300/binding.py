@@ -37,7 +37,7 @@ SIGNATURES = {
     "topk_select_ex": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _P, _P, _P, _P,
                                       _I32, _U64, _U32]),
     "topk_ws_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _P]),
-    "topk_ws_stats": (ctypes.c_int, [_P, _I32, _I64, _I32, _I32, _P, _P, _P]),
+    "topk_ws_stats": (ctypes.c_int, [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P]),
     "topk_visit_order": (ctypes.c_int, [_I32, _I32, _I64, _U64, _P, _P]),
 }
 
@@ -110,12 +110,11 @@ def topk_ws_status(ws, stream=None) -> tuple[int, int]:
 
 
 def topk_ws_stats(ws, rows, n, k, split=0, stream=None):
-    """Returns (rc, survivors list, sorts list) and clears the counters."""
-    surv = (ctypes.c_uint32 * max(rows, 1))()
-    sorts = (ctypes.c_uint32 * max(rows, 1))()
-    rc = int(LIB.topk_ws_stats(_ptr(ws), rows, n, k, split, ctypes.addressof(surv),
-                               ctypes.addressof(sorts), _stream(stream)))
-    return rc, list(surv)[:rows], list(sorts)[:rows]
+    """Returns (rc, survivors, sorts, admitted) per row and clears the counters."""
+    arrs = [(ctypes.c_uint32 * max(rows, 1))() for _ in range(3)]
+    rc = int(LIB.topk_ws_stats(_ptr(ws), rows, n, k, split, *[ctypes.addressof(a) for a in arrs],
+                               _stream(stream)))
+    return (rc, *[list(a)[:rows] for a in arrs])
 
 
 def topk_visit_order(m, row, first_block, seed, order_out, stream=None) -> int:

@@ -10,13 +10,15 @@
 // 32-bit survivor mask 5:10-5:22; the split-row leader merge 5:33-5:45.)
 //
 // GB300 mapping:
-//  * Work is cut into pieces (a run of blocks of one row) and each CTA streams
-//    its pieces through a ring of shared-memory stages.  A producer warp moves
-//    blocks HBM -> shared memory with cp.async.bulk (each stage a few blocks,
-//    signalled by an mbarrier with an expected byte count) and never takes
-//    part in sorting, so loads keep streaming -- across piece boundaries too --
-//    while the consumer warps sort.  Consumers free a stage through a
-//    second mbarrier as soon as its scores are in registers.
+//  * Work is cut into pieces (a run of blocks of one row).  Inside a CTA three
+//    kinds of warps run side by side with no CTA-wide barrier after set-up:
+//    a producer warp moves blocks HBM -> shared memory with cp.async.bulk into
+//    a ring of stages (a few blocks each, signalled by an mbarrier with an
+//    expected byte count); filter warps test every element and append
+//    survivors to a shared-memory inbox ring; selector warps keep the tray,
+//    the kept list and the threshold, build the visiting orders and finish
+//    each piece.  Loads keep streaming -- across piece boundaries too --
+//    while the selectors sort.
 //  * Two plans.  Short batches of full-length rows: a persistent grid of one
 //    CTA per SM, each owning an equal share of the batch's blocks laid end to
 //    end, so every SM streams the same number of bytes; rows that straddle a
@@ -33,13 +35,19 @@
 //    exact word compare runs only for element slots some lane of the warp
 //    flagged (found with one warp OR-reduction).
 //  * Survivors are compacted with __ballot_sync masks and __popc prefixes; one
-//    shared-memory atomicAdd per warp and slot reserves tray space.
-//  * The tray is sorted in batches of max(512, k') words (k' = k rounded up to
-//    a power of two) by a bitonic network that applies up to three strides per
-//    barrier round, then merged into the kept list: the element-wise max of the kept list against the reversed
-//    batch is a bitonic sequence holding the best k' of both, and a bitonic
-//    merge sorts it.  Words still waiting are re-tested against the raised
-//    threshold before the next batch.
+//    shared-memory atomicAdd per warp and stage reserves inbox space.  An
+//    empty inbox slot holds the word 0, which no element packs to, so the
+//    selectors can tell a reserved slot whose word has not landed yet.
+//  * Every 512 new tray words a byte-wise histogram select over kept + tray
+//    finds a word prefix T with at least k words at or above it; tray words
+//    below T can never reach the best k and are dropped, and the threshold
+//    rises to T.  When the tray passes its 2048-word mark, and at the end of
+//    a piece, the survivors are sorted by a bitonic network (up to three
+//    strides per barrier round) and merged into the kept list: the
+//    element-wise max of the kept list against the reversed sorted words is a
+//    bitonic sequence holding the best k' of both (k' = k rounded up to a
+//    power of two), and a bitonic merge sorts it; the threshold becomes the
+//    k-th kept word.
 //  * A split row's CTAs share the best threshold any of them has reached
 //    through a 64-bit atomicMax word per row.  Each publishes its sorted local
 //    top-k to the workspace, fences, and takes a ticket; the CTA that draws the
@@ -48,8 +56,9 @@
 //    DeepSeek V4.1 Flash, kernelbench model page, entry on the split-KV paged
 //    decode), then resets the ticket and threshold word for the next call.
 //  * No kernel ever traps or waits without a bound: bad lengths and NaNs set
-//    workspace status bits, and every mbarrier wait gives up after a fixed
-//    number of polls, setting a status bit.
+//    workspace status bits, and every wait (mbarrier, inbox room, inbox slot,
+//    end of piece) gives up after a fixed number of polls, setting a status
+//    bit; after one wait has given up the others poll once and the CTA drains.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -64,7 +73,9 @@ namespace {
 
 constexpr int kBlock = 1024;          // elements per block ("blocks of 1,024")
 constexpr int kPermChunk = 1024;      // blocks shuffled together
-constexpr int kMinBatch = 512;        // tray sort batch (at least k')
+constexpr int kTrayMark = 2048;       // tray words that trigger the tray sort
+constexpr int kPruneStep = 512;       // new tray words that trigger a prune
+constexpr int kSelectSlack = 256;     // extra words a pruned tray may keep
 constexpr int kMaxSplit = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait gives up
 
@@ -77,25 +88,39 @@ constexpr int kManyRows = kSms;       // rows per call from which each gets a CT
 
 constexpr uint64_t kDefaultSeed = 0x5EEDC0DE1234ABCDull;
 
-// CTA shapes: consumer warps, blocks per ring stage, ring stages, CTAs/SM.
-template <int NW_, int BPS_, int NSTAGE_, int MINB_>
+// CTA shapes: filter warps, selector warps, blocks per ring stage, ring
+// stages, CTAs per SM to fit registers for, inbox and tray capacities (words).
+template <int NF_, int NS_, int BPS_, int NSTAGE_, int MINB_, int INBOX_, int TRAY_>
 struct Shape {
-  static constexpr int NW = NW_;
+  static constexpr int NF = NF_;
+  static constexpr int NS = NS_;
   static constexpr int BPS = BPS_;
   static constexpr int NSTAGE = NSTAGE_;
   static constexpr int MIN_BLOCKS = MINB_;
-  static constexpr int NC = NW * 32;               // consumer threads
-  static constexpr int NTHREADS = NC + 32;         // plus the producer warp
-  static constexpr int EPT = BPS * kBlock / NC;    // elements per thread per stage
-  static constexpr int F4 = EPT / 4;               // float4 loads per thread per stage
+  static constexpr int INBOX = INBOX_;
+  static constexpr int TRAY = TRAY_;
+  static constexpr int NFT = NF * 32;               // filter threads
+  static constexpr int NST = NS * 32;               // selector threads
+  static constexpr int NTHREADS = NFT + NST + 32;   // plus the producer warp
+  static constexpr int PRODUCER_WARP = NF + NS;
   static constexpr int STAGE_FLOATS = BPS * kBlock;
-  static_assert(EPT % 4 == 0, "whole float4s per thread");
-  static_assert(EPT <= 32, "candidate bits fit one word");
-  static_assert(NC == 256 || NC == 512, "batch sorts are instantiated for 256 or 512 consumers");
+  static constexpr int EPT = STAGE_FLOATS / NFT;    // elements per filter thread per stage
+  static constexpr int F4 = EPT / 4;                // float4 loads per filter thread per stage
+  // Inbox words the selectors move per step.  A take must never reach a slot
+  // reserved by a filter warp that is itself waiting for room, so it stays at
+  // least one warp-stage reservation (32 * EPT words) short of the ring size.
+  static constexpr int TAKE_MAX =
+      (INBOX - 32 * EPT) < 1024 ? (INBOX - 32 * EPT) : 1024;
+  static_assert(EPT % 4 == 0 && EPT <= 32, "whole float4s, candidate bits in one word");
+  static_assert((INBOX & (INBOX - 1)) == 0, "inbox ring size is a power of two");
+  static_assert(TAKE_MAX >= 256, "inbox leaves room for a take");
+  static_assert(TRAY >= kTrayMark + 512 && TRAY >= TAKE_MAX, "tray holds a take past its mark");
 };
 
-using BigShape = Shape<16, 4, 8, 1>;    // 544 threads, 128 KB ring, 1 CTA/SM
-using SmallShape = Shape<8, 1, 8, 3>;   // 288 threads, 32 KB ring, 3 CTAs/SM
+using BigShape = Shape<8, 8, 4, 8, 1, 4096, 3072>;    // 544 threads, 128 KB ring, 1 CTA/SM
+using SmallShape = Shape<4, 4, 1, 8, 2, 1024, 2560>;  // 288 threads, 32 KB ring
+
+constexpr uint32_t kNoBlock = 0xFFFFFFFFu;  // descriptor of an empty stage slot
 
 // Plans.
 constexpr int kPlanRows = 0;   // CTA = (row, segment)
@@ -105,15 +130,17 @@ constexpr int kPlanFlat = 1;   // CTA = equal share of the batch's blocks
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)              header: u32 status
 //   tickets   u32[rows]   split-row leader election, zero between calls
-//   survivors u32[rows]   elements admitted to a tray, per row (accumulating)
-//   sorts     u32[rows]   tray sort batches per row (accumulating)
+//   survivors u32[rows]   tray words that entered a bitonic tray sort, per row
+//   sorts     u32[rows]   bitonic tray sorts per row
+//   admitted  u32[rows]   elements that passed the threshold test, per row
+//                         (the three counters accumulate until read)
 //   theta     u64[rows]   split rows: best threshold word any of the row's CTAs
 //                         has reached, zero between calls
 //   partials  u64[slots][kp]  local top-k lists of split rows; slots =
 //                         max(rows * split, 2 * kMaxFlatCtas) when rows can
 //                         be split, else none
 struct WsLayout {
-  size_t tickets, survivors, sorts, theta, partials, total;
+  size_t tickets, survivors, sorts, admitted, theta, partials, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -159,6 +186,8 @@ WsLayout ws_layout(int32_t rows, int32_t kp, size_t slots) {
   off = align256(off + sizeof(uint32_t) * size_t(rows));
   L.sorts = off;
   off = align256(off + sizeof(uint32_t) * size_t(rows));
+  L.admitted = off;
+  off = align256(off + sizeof(uint32_t) * size_t(rows));
   L.theta = off;
   off = align256(off + sizeof(uint64_t) * size_t(rows));
   L.partials = off;
@@ -178,7 +207,6 @@ struct Params {
   int32_t rows;
   int32_t k;
   int32_t kp;          // next power of two >= k: kept-list capacity
-  int32_t batch;       // tray sort batch: max(kMinBatch, kp)
   int32_t plan;        // kPlanRows or kPlanFlat
   int32_t split;       // kPlanRows: CTAs per row
   int32_t seg_blocks;  // kPlanRows: blocks per segment
@@ -189,6 +217,7 @@ struct Params {
   uint32_t* tickets;
   uint32_t* survivors;
   uint32_t* sorts;
+  uint32_t* admitted;
   unsigned long long* row_theta;
   uint64_t* partials;
   uint32_t seed_lo, seed_hi;
@@ -196,24 +225,28 @@ struct Params {
 };
 
 struct SmemLayout {
-  int ring, kept, fresh, perm, bars, total;
+  int ring, desc, inbox, tray, kept, perm, hist, bars, total;
 };
-
-__host__ __device__ inline int batch_of(int kp) { return kp > kMinBatch ? kp : kMinBatch; }
 
 template <class S>
 __host__ __device__ inline SmemLayout smem_layout(int kp) {
-  const int batch = batch_of(kp);
   SmemLayout L;
   int off = 0;
   L.ring = off;
   off += S::NSTAGE * S::STAGE_FLOATS * int(sizeof(float));
+  L.desc = off;
+  off += S::NSTAGE * S::BPS * int(sizeof(uint32_t));
+  off = (off + 15) & ~15;
+  L.inbox = off;  // inbox and tray are contiguous: the leader merge uses both
+  off += S::INBOX * int(sizeof(uint64_t));
+  L.tray = off;
+  off += S::TRAY * int(sizeof(uint64_t));
   L.kept = off;
   off += kp * int(sizeof(uint64_t));
-  L.fresh = off;
-  off += (batch + S::STAGE_FLOATS) * int(sizeof(uint64_t));
   L.perm = off;
   off += 2 * kPermChunk * int(sizeof(uint32_t));
+  L.hist = off;
+  off += 256 * int(sizeof(uint32_t));
   L.bars = off;
   off += (2 * S::NSTAGE + 2) * int(sizeof(uint64_t));
   L.total = off;
@@ -221,11 +254,17 @@ __host__ __device__ inline SmemLayout smem_layout(int kp) {
 }
 
 struct CtaState {
-  int cnt;          // words waiting in the tray
-  int cnt2;         // scratch counter for re-filtering
-  int leader;       // this CTA drew the last ticket
-  int ragged[2];    // per visit-order buffer: position of the ragged block, or -1
-  uint64_t theta;   // the threshold word (0 = nothing kept yet)
+  uint32_t head;      // inbox: next word the selectors take
+  uint32_t tail;      // inbox: next word a filter warp reserves
+  int fdone;          // filter warps done with the current piece
+  int piece_gen;      // pieces the selectors have finished
+  int prod_chunk;     // chunk the producer is streaming
+  int flags;          // selector broadcast scratch
+  int cnt2;           // compaction counter
+  int leader;         // this CTA drew the last ticket
+  int sel_b, sel_above, sel_binc;  // histogram select: chosen bin and counts
+  int sel_n, sel_done;             // selector step: words to take, piece done
+  uint64_t theta;     // the threshold word the filters test against
 };
 
 // A piece: blocks [b_begin, b_end) of row r, processed with one tray.
@@ -338,24 +377,17 @@ __device__ void build_visit_order(uint32_t* perm, int cs, int64_t first, int32_t
   bitonic_network<T, uint32_t, false>(perm, p2, 2, 1, 0, t);
 }
 
-// Merge the first kp words of a sorted-descending `batch` into the kept list:
-// the best kp of both end up sorted in kept.
+// Merge a sorted-descending `batch` of n words (read as if padded with empty
+// words to kp) into the kept list: the best kp of both end up sorted in kept.
 template <class T>
-__device__ void merge_into_kept(uint64_t* kept, const uint64_t* batch, int kp, int t) {
+__device__ void merge_into_kept(uint64_t* kept, const uint64_t* batch, int n, int kp, int t) {
   for (int j = t; j < kp; j += T::size) {
-    const uint64_t a = kept[j], b = batch[kp - 1 - j];
+    const int i = kp - 1 - j;
+    const uint64_t a = kept[j], b = i < n ? batch[i] : 0ull;
     kept[j] = a > b ? a : b;
   }
   T::sync();
   bitonic_network<T, uint64_t, true>(kept, kp, kp, 1, 0, t);
-}
-
-// Sorts the first B tray words (descending, in place) and merges the first
-// kp of them into the kept list.  Entered right after a team barrier.
-template <class T>
-__device__ void sort_batch(int B, uint64_t* fresh, uint64_t* kept, int kp, int t) {
-  bitonic_network<T, uint64_t, true>(fresh, B, 2, 1, 0, t);
-  merge_into_kept<T>(kept, fresh, kp, t);
 }
 
 __device__ __forceinline__ void write_row(const Params& p, int32_t r, const uint64_t* kept, int t,
@@ -376,16 +408,30 @@ __device__ __forceinline__ void write_row(const Params& p, int32_t r, const uint
 
 // ---------------------------------------------------------------------------
 // The selection kernel.
+//
+// Roles inside a CTA (no CTA-wide barrier after set-up):
+//  * the producer warp (lane 0) streams each stage's blocks with
+//    cp.async.bulk and writes the stage's block descriptors;
+//  * NF filter warps test every element against the current threshold and
+//    append survivors to a shared-memory inbox ring (empty slots hold the
+//    word 0, which no element ever packs to, so a reader can tell a slot that
+//    is reserved but not yet written);
+//  * NS selector warps drain the inbox into the tray, raise the threshold
+//    (histogram select + prune), run the bitonic tray sort when the tray
+//    passes its mark, build the visiting orders and finish each piece.
 
 template <class S>
 __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel(const Params p) {
-  using Cons = Team<S::NC, 1>;
+  using Sel = Team<S::NST, 1>;
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout sl = smem_layout<S>(p.kp);
   float* ring = reinterpret_cast<float*>(smem + sl.ring);
+  uint32_t* desc = reinterpret_cast<uint32_t*>(smem + sl.desc);
+  uint64_t* inbox = reinterpret_cast<uint64_t*>(smem + sl.inbox);
+  uint64_t* tray = reinterpret_cast<uint64_t*>(smem + sl.tray);
   uint64_t* kept = reinterpret_cast<uint64_t*>(smem + sl.kept);
-  uint64_t* fresh = reinterpret_cast<uint64_t*>(smem + sl.fresh);
   uint32_t* perm = reinterpret_cast<uint32_t*>(smem + sl.perm);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + sl.hist);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + sl.bars);
   uint64_t* empty = full + S::NSTAGE;
   uint64_t* perm_ready = empty + S::NSTAGE;
@@ -395,7 +441,7 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const bool identity = (p.flags & TOPK_FLAG_IDENTITY_ORDER) != 0;
-  const int kp = p.kp, k = p.k, B = p.batch;
+  const int kp = p.kp, k = p.k;
 
   // a1: lengths outside [0, n] are clamped and reported once per row.
   if (p.plan == kPlanRows && p.lengths && tid == 0 && blockIdx.x % uint32_t(p.split) == 0) {
@@ -414,15 +460,18 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
   }
 
   for (int j = tid; j < kp; j += S::NTHREADS) kept[j] = 0ull;
+  for (int j = tid; j < S::INBOX; j += S::NTHREADS) inbox[j] = 0ull;
   if (tid == 0) {
-    st.cnt = 0;
-    st.cnt2 = 0;
+    st.head = 0;
+    st.tail = 0;
+    st.fdone = 0;
+    st.piece_gen = 0;
+    st.prod_chunk = -1;
     st.theta = 0ull;
-    st.leader = 0;
-    st.ragged[0] = st.ragged[1] = -1;
+    st.flags = 0;
     for (int i = 0; i < S::NSTAGE; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], S::NW);
+      mbar_init(&empty[i], S::NF);
     }
     mbar_init(&perm_ready[0], 1);
     mbar_init(&perm_ready[1], 1);
@@ -430,8 +479,8 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
   }
   __syncthreads();
 
-  // ---------------- producer warp: a3, the bulk-copy stream ----------------
-  if (warp == S::NW) {
+  // ---------------- producer: a3, the bulk-copy stream ----------------
+  if (warp == S::PRODUCER_WARP) {
     if (lane != 0) return;
     bool gave_up = false;
     uint32_t g = 0;
@@ -441,6 +490,8 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
       const float* row = p.scores + int64_t(cur.pc.r) * p.row_stride;
       const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
       if (!mbar_wait(&perm_ready[c & 1], (c >> 1) & 1, gave_up ? 1u : kWaitLimit)) gave_up = true;
+      // the buffer of chunk c - 1 is no longer read: the selectors may refill it
+      *reinterpret_cast<volatile int*>(&st.prod_chunk) = c;
       for (int i = 0; i < cur.cs; i += S::BPS, ++g) {
         const uint32_t stage = g % S::NSTAGE;
         if (g >= uint32_t(S::NSTAGE) &&
@@ -453,12 +504,16 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
         for (int b = 0; b < S::BPS; ++b) {
           bytes[b] = 0;
           src[b] = row;
-          if (i + b < cur.cs && aligned) {
-            const uint32_t e0 = uint32_t(cur.cb + int32_t(pc[i + b] & 1023u)) * kBlock;
-            const uint32_t valid = min(uint32_t(kBlock), cur.pc.L - e0);
-            bytes[b] = (valid & ~3u) * 4u;
-            src[b] = row + e0;
+          uint32_t e0 = kNoBlock;
+          if (i + b < cur.cs) {
+            e0 = uint32_t(cur.cb + int32_t(pc[i + b] & 1023u)) * kBlock;
+            if (aligned) {
+              const uint32_t valid = min(uint32_t(kBlock), cur.pc.L - e0);
+              bytes[b] = (valid & ~3u) * 4u;
+              src[b] = row + e0;
+            }
           }
+          desc[stage * S::BPS + b] = e0;
           total += bytes[b];
         }
         fence_proxy_async_smem();
@@ -478,121 +533,439 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
     return;
   }
 
-  // ---------------- consumer warps ----------------
-  const int ct = tid;  // 0 .. NC-1
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  uint64_t th = 0ull;
-  float thf = threshold_float(th);
-  uint32_t admitted = 0, nsorts = 0;
-  bool saw_nan = false, timed_out = false;
-  uint32_t g = 0;
-  bool shared_theta = false;
-  int32_t row_r = 0;
-
-  // a2: the visiting order of a chunk, and where the row's ragged last block
-  // (if any) falls in it.
-  auto build_order = [&](const Cursor& cu, int buf) {
-    uint32_t* pb = perm + buf * kPermChunk;
-    build_visit_order<Cons>(pb, cu.cs, cu.cb, cu.pc.r, p.seed_lo, p.seed_hi, identity, ct);
-    const int32_t ragged_blk = (cu.pc.L & (kBlock - 1)) ? cu.pc.m - 1 : -1;
-    if (ct == 0) st.ragged[buf] = -1;
-    Cons::sync();
-    if (ragged_blk >= cu.cb && ragged_blk < cu.cb + cu.cs) {
-      for (int j = ct; j < cu.cs; j += S::NC)
-        if (int32_t(pb[j] & 1023u) == ragged_blk - cu.cb) st.ragged[buf] = j;
-    }
-    Cons::sync();
-    if (ct == 0) mbar_arrive(&perm_ready[buf]);
-  };
-
-  // a6: sort batches of B tray words into the kept list until fewer than B
-  // wait, raising the threshold and re-testing the waiting words after each.
-  auto sort_batches = [&]() {
-    for (;;) {
-      const int cnt = st.cnt;
-      if (cnt < B) break;
-      ++nsorts;
-      sort_batch<Cons>(B, fresh, kept, kp, ct);
-      uint64_t nth = kept[k - 1];
-      const uint64_t cur = st.theta;
-      nth = nth > cur ? nth : cur;
-      uint64_t w[S::EPT];
-      bool keep[S::EPT];
+  // ---------------- filter warps: a4 + a5 ----------------
+  if (warp < S::NF) {
+    const int ft = tid;  // 0 .. NFT-1
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    uint64_t th = 0ull;
+    float thf = threshold_float(th);
+    uint32_t admitted = 0;
+    bool saw_nan = false, timed_out = false;
+    int gen = 0;
+    uint32_t g = 0;
+    Cursor cur = first;
+    for (int c = 0; cur.valid; ++c) {
+      const float* row = p.scores + int64_t(cur.pc.r) * p.row_stride;
+      const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+      const uint32_t L32 = cur.pc.L;
+      const int cs = cur.cs;
+      for (int i = 0; i < cs; i += S::BPS, ++g) {
+        const uint32_t stage = g % S::NSTAGE;
+        if (!mbar_wait(&full[stage], (g / S::NSTAGE) & 1, timed_out ? 1u : kWaitLimit))
+          timed_out = true;
+        const uint64_t nt = *reinterpret_cast<volatile uint64_t*>(&st.theta);
+        if (nt != th) {
+          th = nt;
+          thf = threshold_float(th);
+        }
+        const float* src = ring + stage * S::STAGE_FLOATS;
+        uint32_t e0s[S::F4];
+        bool clean = aligned;
 #pragma unroll
-      for (int u = 0; u < S::EPT; ++u) {
-        const int t = B + ct + u * S::NC;
-        w[u] = t < cnt ? fresh[t] : 0ull;
-        keep[u] = w[u] > nth;
-      }
-      Cons::sync();  // every waiting word is in registers
+        for (int u = 0; u < S::F4; ++u) {
+          const uint32_t e0 = desc[stage * S::BPS + ((ft + S::NFT * u) >> 8)];
+          e0s[u] = e0;
+          clean &= e0 != kNoBlock && e0 + kBlock <= L32;
+        }
+        float x[S::EPT];
+        uint32_t cand = 0;  // bit e: element e may beat the threshold
+        if (clean) {
 #pragma unroll
-      for (int u = 0; u < S::EPT; ++u) {
-        const uint32_t mask = __ballot_sync(0xFFFFFFFFu, keep[u]);
-        if (mask) {
-          int base = 0;
-          if (lane == 0) base = atomicAdd(&st.cnt2, __popc(mask));
-          base = __shfl_sync(0xFFFFFFFFu, base, 0);
-          if (keep[u]) fresh[base + __popc(mask & lt_mask)] = w[u];
+          for (int u = 0; u < S::F4; ++u) {
+            const float4 v = reinterpret_cast<const float4*>(src)[ft + S::NFT * u];
+            x[4 * u + 0] = v.x;
+            x[4 * u + 1] = v.y;
+            x[4 * u + 2] = v.z;
+            x[4 * u + 3] = v.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[stage]);
+          // One question per element.  The float compare passes a superset of
+          // the exact survivors (equal values, NaN); the word compare decides.
+#pragma unroll
+          for (int e = 0; e < S::EPT; ++e) cand |= uint32_t(!(x[e] < thf)) << e;
+        } else {
+#pragma unroll
+          for (int u = 0; u < S::F4; ++u) {
+            const int q = ft + S::NFT * u;
+            const int b = q >> 8;
+            const uint32_t j0 = uint32_t((q & 255) * 4);
+            const uint32_t e0 = e0s[u];
+            uint32_t valid = 0, copied = 0;
+            if (e0 != kNoBlock) {
+              valid = min(uint32_t(kBlock), L32 - e0);
+              copied = aligned ? (valid & ~3u) : 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t j = j0 + uint32_t(e);
+              float v = 0.f;
+              if (j < copied) v = src[b * kBlock + j];
+              else if (j < valid) v = __ldg(row + e0 + j);
+              x[4 * u + e] = v;
+              if (j < valid) cand |= uint32_t(!(v < thf)) << (4 * u + e);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[stage]);
+        }
+
+        const uint32_t wcand = __reduce_or_sync(0xFFFFFFFFu, cand);
+        if (wcand) {
+          // For each element slot some lane flagged: the exact word test and a
+          // ballot mask; then one inbox reservation for the warp and the writes
+          // at __popc prefix offsets.
+          uint32_t pm[S::EPT];
+          int total = 0;
+#pragma unroll
+          for (int e = 0; e < S::EPT; ++e) {
+            pm[e] = 0u;
+            if ((wcand >> e) & 1u) {
+              bool pass = false;
+              if ((cand >> e) & 1u) {
+                const uint32_t bits = __float_as_uint(x[e]);
+                const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+                saw_nan |= nan;
+                const uint32_t idx = e0s[e >> 2] + uint32_t(((ft + S::NFT * (e >> 2)) & 255) * 4 + (e & 3));
+                const uint64_t w = (uint64_t(order_key(bits)) << 32) | uint64_t(~idx);
+                pass = !nan && w > th;
+              }
+              pm[e] = __ballot_sync(0xFFFFFFFFu, pass);
+              total += __popc(pm[e]);
+            }
+          }
+          if (total) {
+            uint32_t pos = 0;
+            if (lane == 0) {
+              pos = atomicAdd(&st.tail, uint32_t(total));
+              admitted += uint32_t(total);
+              // wait for room: the selectors free slots by advancing head
+              uint32_t it = timed_out ? kWaitLimit : 0u;
+              while (pos + uint32_t(total) - *reinterpret_cast<volatile uint32_t*>(&st.head) >
+                     uint32_t(S::INBOX)) {
+                if (++it > kWaitLimit) {
+                  timed_out = true;
+                  break;
+                }
+                __nanosleep(64);
+              }
+            }
+            pos = __shfl_sync(0xFFFFFFFFu, pos, 0);
+#pragma unroll
+            for (int e = 0; e < S::EPT; ++e) {
+              if (pm[e]) {
+                if ((pm[e] >> lane) & 1u) {
+                  const uint32_t bits = __float_as_uint(x[e]);
+                  const uint32_t idx = e0s[e >> 2] + uint32_t(((ft + S::NFT * (e >> 2)) & 255) * 4 + (e & 3));
+                  const uint64_t w = (uint64_t(order_key(bits)) << 32) | uint64_t(~idx);
+                  reinterpret_cast<volatile uint64_t*>(inbox)[(pos + __popc(pm[e] & lt_mask)) &
+                                                              (S::INBOX - 1)] = w;
+                }
+                pos += __popc(pm[e]);
+              }
+            }
+          }
         }
       }
-      if (ct == 0 && shared_theta) {
-        // share the raised threshold with the row's other CTAs
-        const unsigned long long old = atomicMax(&p.row_theta[row_r], (unsigned long long)nth);
-        if (old > nth) nth = old;
+      Cursor nxt = cur;
+      cursor_next(p, nxt);
+      if (!nxt.valid || nxt.pi != cur.pi) {
+        // end of a piece: report, then wait until the selectors have finished
+        // it before filtering the next piece with a fresh threshold
+        __syncwarp();
+        if (lane == 0) {
+          if (admitted) atomicAdd(&p.admitted[cur.pc.r], admitted);
+          __threadfence_block();
+          atomicAdd(&st.fdone, 1);
+        }
+        admitted = 0;
+        ++gen;
+        if (nxt.valid) {
+          uint32_t it = timed_out ? kWaitLimit : 0u;
+          while (*reinterpret_cast<volatile int*>(&st.piece_gen) < gen) {
+            if (++it > kWaitLimit) {
+              timed_out = true;
+              break;
+            }
+            __nanosleep(128);
+          }
+          __syncwarp();
+          th = *reinterpret_cast<volatile uint64_t*>(&st.theta);
+          thf = threshold_float(th);
+        }
       }
-      Cons::sync();
-      if (ct == 0) {
-        st.cnt = st.cnt2;
-        st.cnt2 = 0;
-        st.theta = nth;
+      cur = nxt;
+    }
+    saw_nan = __any_sync(0xFFFFFFFFu, saw_nan);
+    timed_out = __any_sync(0xFFFFFFFFu, timed_out);
+    if (lane == 0) {
+      if (saw_nan) atomicOr(p.status, TOPK_STATUS_NAN);
+      if (timed_out) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
+    }
+    return;
+  }
+
+  // ---------------- selector warps: a2, a6, a7, a8 ----------------
+  const int stt = tid - S::NFT;  // 0 .. NST-1
+  const int swarp = stt >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  bool timed_out = false;
+  uint32_t nsorts = 0, nsorted = 0;
+  int tray_n = 0;       // words in the tray
+  int kept_n = 0;       // real words in the kept list
+  int pruned = 0;       // tray words left by the last prune
+  uint64_t theta = 0ull;
+  uint32_t head = 0;
+
+  // a2: visiting orders are built ahead of the producer, one chunk at a time
+  Cursor bcur = first;
+  int built = 0;
+  auto build_next = [&]() {
+    uint32_t* pb = perm + (built & 1) * kPermChunk;
+    build_visit_order<Sel>(pb, bcur.cs, bcur.cb, bcur.pc.r, p.seed_lo, p.seed_hi, identity, stt);
+    if (stt == 0) mbar_arrive(&perm_ready[built & 1]);
+    ++built;
+    cursor_next(p, bcur);
+  };
+  build_next();
+
+  // Publish a threshold to the filters (and to the row's other CTAs).
+  auto raise_theta = [&](uint64_t nth, const Piece& pc) {
+    if (nth <= theta) return;
+    theta = nth;
+    if (stt == 0) {
+      if (pc.contributors > 1) {
+        const unsigned long long old = atomicMax(&p.row_theta[pc.r], (unsigned long long)nth);
+        if (old > nth) theta = old;
       }
-      Cons::sync();
+      *reinterpret_cast<volatile uint64_t*>(&st.theta) = theta;
     }
   };
 
-  // End of a piece: final sort, then the row's output (directly, or through
-  // the split-row ticket), then a clean tray for the next piece.
-  auto finish_piece = [&](const Piece& pc) {
-    const int cnt = st.cnt;
-    if (cnt > 0) {
-      ++nsorts;
-      for (int t = cnt + ct; t < B; t += S::NC) fresh[t] = 0ull;
-      Cons::sync();
-      sort_batch<Cons>(B, fresh, kept, kp, ct);
+  // a6: the tray.  A byte-wise histogram select over kept + tray finds a word
+  // prefix T such that at least k words are >= T and at most kp + slack are;
+  // tray words below T can never reach the best k and are dropped, and the
+  // threshold rises to T.  With `sort` (the tray has passed its mark, or the
+  // piece is done) the rest are bitonic-sorted and merged into the kept
+  // list, whose k-th word becomes the threshold, and the tray is emptied.
+  auto process_tray = [&](bool sort, const Piece& pc) {
+    const int slack = kp >= kTrayMark ? 0 : kSelectSlack;
+    uint64_t T = 0ull;
+    if (kept_n + tray_n > kp + slack) {
+      uint64_t prefix = 0ull;
+      uint32_t need = uint32_t(k), greater = 0;
+      for (int pass = 0; pass < 8; ++pass) {
+        const int shift = 56 - 8 * pass;
+        const uint64_t hmask = pass == 0 ? 0ull : (~0ull << (shift + 8));
+        for (int b = stt; b < 256; b += S::NST) hist[b] = 0u;
+        Sel::sync();
+        for (int j = stt; j < kp + tray_n; j += S::NST) {
+          const uint64_t w = j < kp ? kept[j] : tray[j - kp];
+          if (w != 0ull && (w & hmask) == prefix) atomicAdd(&hist[(w >> shift) & 0xFFu], 1u);
+        }
+        Sel::sync();
+        if (swarp == 0) {
+          // lane l owns bins 255-8l .. 248-8l, scanned from the top
+          uint32_t cnt8[8], sum = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            cnt8[q] = hist[255 - 8 * lane - q];
+            sum += cnt8[q];
+          }
+          uint32_t incl = sum;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= d) incl += o;
+          }
+          const uint32_t excl = incl - sum;
+          if (excl < need && incl >= need) {
+            uint32_t acc = excl;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (acc < need && acc + cnt8[q] >= need) {
+                st.sel_b = 255 - 8 * lane - q;
+                st.sel_above = int(acc);
+                st.sel_binc = int(cnt8[q]);
+              }
+              acc += cnt8[q];
+            }
+          }
+        }
+        Sel::sync();
+        const uint32_t b = uint32_t(st.sel_b);
+        const uint32_t above = uint32_t(st.sel_above), binc = uint32_t(st.sel_binc);
+        prefix |= uint64_t(b) << shift;
+        greater += above;
+        need -= above;
+        if (greater + binc <= uint32_t(kp + slack) || pass == 7) {
+          T = prefix;
+          break;
+        }
+      }
     }
-    if (lane == 0 && admitted) atomicAdd(&p.survivors[pc.r], admitted);
-    admitted = 0;
-    if (ct == 0) atomicAdd(&p.sorts[pc.r], nsorts);
-    nsorts = 0;
+    // keep the tray words >= T, compacting in rounds that never overwrite a
+    // word not yet read (a kept word only moves to a lower position)
+    if (stt == 0) st.cnt2 = 0;
+    Sel::sync();
+    constexpr int R = 8;
+    for (int base0 = 0; base0 < tray_n; base0 += R * S::NST) {
+      uint64_t w[R];
+      bool keep[R];
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        const int t = base0 + u * S::NST + stt;
+        w[u] = t < tray_n ? tray[t] : 0ull;
+        keep[u] = w[u] != 0ull && w[u] >= T;
+      }
+      Sel::sync();
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        const uint32_t mask = __ballot_sync(0xFFFFFFFFu, keep[u]);
+        if (mask) {
+          int at = 0;
+          if (lane == 0) at = atomicAdd(&st.cnt2, __popc(mask));
+          at = __shfl_sync(0xFFFFFFFFu, at, 0);
+          if (keep[u]) tray[at + __popc(mask & lt_mask)] = w[u];
+        }
+      }
+    }
+    Sel::sync();
+    const int r = st.cnt2;
+    if (!sort) {
+      tray_n = r;
+      pruned = r;
+      raise_theta(T ? T - 1ull : 0ull, pc);
+      return;
+    }
+    // the bitonic tray sort: sort the r survivors and merge them in
+    const int P = next_pow2_dev(max(r, 1));
+    for (int t = r + stt; t < P; t += S::NST) tray[t] = 0ull;
+    Sel::sync();
+    bitonic_network<Sel, uint64_t, true>(tray, P, 2, 1, 0, stt);
+    merge_into_kept<Sel>(kept, tray, P, kp, stt);
+    ++nsorts;
+    nsorted += uint32_t(r);
+    kept_n = min(kp, kept_n + r);
+    tray_n = 0;
+    pruned = 0;
+    raise_theta(kept[k - 1], pc);
+  };
 
+  // Move up to `n` reserved inbox words into the tray (a slot still 0 is
+  // reserved but not yet written: wait for it), and free their slots.
+  auto take = [&](int n) {
+    for (int j = stt; j < n; j += S::NST) {
+      volatile uint64_t* slot =
+          reinterpret_cast<volatile uint64_t*>(inbox) + ((head + uint32_t(j)) & (S::INBOX - 1));
+      uint64_t w = *slot;
+      uint32_t it = timed_out ? kWaitLimit : 0u;
+      while (w == 0ull) {
+        if (++it > kWaitLimit) {
+          timed_out = true;
+          break;
+        }
+        __nanosleep(32);
+        w = *slot;
+      }
+      *slot = 0ull;
+      tray[tray_n + j] = w;
+    }
+    __threadfence_block();  // the emptied slots are visible before head moves
+    Sel::sync();
+    head += uint32_t(n);
+    tray_n += n;
+    if (stt == 0) *reinterpret_cast<volatile uint32_t*>(&st.head) = head;
+  };
+
+  Cursor pcur = first;  // the piece being selected
+  int piece_no = 0;
+  while (pcur.valid) {
+    const Piece pc = pcur.pc;
+    uint32_t idle = 0;
+    for (;;) {
+      // build the next visiting order once the producer no longer reads its buffer
+      if (bcur.valid) {
+        if (stt == 0)
+          st.flags = (*reinterpret_cast<volatile int*>(&st.prod_chunk) >= built - 1) ? 1 : 0;
+        Sel::sync();
+        const bool go = st.flags != 0;
+        Sel::sync();
+        if (go) build_next();
+      }
+      // what is waiting: read the finished-filter count before the tail, so a
+      // full count means the tail is final
+      if (stt == 0) {
+        const int fd = *reinterpret_cast<volatile int*>(&st.fdone);
+        const uint32_t tail = *reinterpret_cast<volatile uint32_t*>(&st.tail);
+        const uint32_t avail = tail - head;
+        int n = int(min(avail, uint32_t(S::TRAY - tray_n)));
+        if (n > S::TAKE_MAX) n = S::TAKE_MAX;
+        st.sel_n = n;
+        st.sel_done = (fd == S::NF && avail == 0) ? 1 : 0;
+        if (pc.contributors > 1) {
+          const unsigned long long gt =
+              *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[pc.r]);
+          if (gt > theta) *reinterpret_cast<volatile uint64_t*>(&st.theta) = gt;
+        }
+      }
+      Sel::sync();
+      const int n = st.sel_n;
+      const bool done = st.sel_done != 0;
+      theta = *reinterpret_cast<volatile uint64_t*>(&st.theta);
+      Sel::sync();
+      if (done) break;
+      if (n > 0) {
+        idle = 0;
+        take(n);
+        if (tray_n >= kTrayMark) process_tray(true, pc);
+        else if (tray_n >= pruned + kPruneStep) process_tray(false, pc);
+      } else {
+        if (++idle > kWaitLimit) {
+          timed_out = true;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+
+    // end of the piece: final sort, then the row's output (directly, or
+    // through the split-row ticket)
+    if (tray_n > 0) process_tray(true, pc);
+    if (stt == 0) {
+      atomicAdd(&p.sorts[pc.r], nsorts);
+      atomicAdd(&p.survivors[pc.r], nsorted);
+    }
+    nsorts = 0;
+    nsorted = 0;
     if (pc.contributors == 1) {
-      write_row(p, pc.r, kept, ct, S::NC);
+      write_row(p, pc.r, kept, stt, S::NST);
     } else {
       // a7: publish the local list, take a ticket; the last ticket merges.
       uint64_t* mine = p.partials + int64_t(pc.slot) * kp;
-      for (int j = ct; j < kp; j += S::NC) mine[j] = kept[j];
+      for (int j = stt; j < kp; j += S::NST) mine[j] = kept[j];
       __threadfence();
-      Cons::sync();
-      if (ct == 0) {
+      Sel::sync();
+      if (stt == 0) {
         const uint32_t t = atomicAdd(&p.tickets[pc.r], 1u);
-        st.leader = (t == uint32_t(pc.contributors - 1));
+        st.leader = (t == uint32_t(pc.contributors - 1)) ? 1 : 0;
       }
-      Cons::sync();
+      Sel::sync();
       if (st.leader) {
         __threadfence();
-        // Gather lists into the idle tray and merge them as a tree of
+        // Gather lists into the idle inbox + tray and merge them as a tree of
         // parallel pairwise merges; the running result stays in slot 0.
-        uint64_t* slots = fresh;
-        const int cap = (B + S::STAGE_FLOATS) / kp;
-        for (int j = ct; j < kp; j += S::NC) slots[j] = kept[j];
+        uint64_t* slots = inbox;  // inbox and tray are contiguous
+        const int cap = (S::INBOX + S::TRAY) / kp;
+        for (int j = stt; j < kp; j += S::NST) slots[j] = kept[j];
         int next_other = 0;  // next contributor to gather (never this CTA)
         const int self = p.plan == kPlanRows ? int(blockIdx.x % uint32_t(p.split))
                                              : int(blockIdx.x) - pc.first_cta;
         int remaining = pc.contributors - 1;
         while (remaining > 0) {
-          const int take = min(remaining, cap - 1);
+          const int takeq = min(remaining, cap - 1);
           int o = next_other;
-          for (int q = 1; q <= take; ++q, ++o) {
+          for (int q = 1; q <= takeq; ++q, ++o) {
             if (o == self) ++o;
             int64_t slot;
             if (p.plan == kPlanRows) {
@@ -603,177 +976,58 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
               slot = 2 * go + (flat_lo(go, M, G) / p.m_full == pc.r ? 0 : 1);
             }
             const uint64_t* other = p.partials + slot * kp;
-            for (int j = ct; j < kp; j += S::NC) slots[q * kp + j] = __ldcg(other + j);
+            for (int j = stt; j < kp; j += S::NST) slots[q * kp + j] = __ldcg(other + j);
           }
           next_other = o;
-          remaining -= take;
-          Cons::sync();
-          const int nl = take + 1;
+          remaining -= takeq;
+          Sel::sync();
+          const int nl = takeq + 1;
           for (int gap = 1; gap < nl; gap <<= 1) {
             // pairs (q, q + gap) for q a multiple of 2*gap with q + gap < nl
             const int npairs = (nl - gap + 2 * gap - 1) / (2 * gap);
-            for (int u = ct; u < npairs * kp; u += S::NC) {
+            for (int u = stt; u < npairs * kp; u += S::NST) {
               const int pr = u / kp, j = u - pr * kp;
               uint64_t* a = slots + (2 * gap * pr) * kp;
               const uint64_t* b = a + gap * kp;
               const uint64_t x = a[j], y = b[kp - 1 - j];
               a[j] = x > y ? x : y;
             }
-            Cons::sync();
-            bitonic_network<Cons, uint64_t, true>(slots, kp, kp, npairs, 2 * gap * kp, ct);
+            Sel::sync();
+            bitonic_network<Sel, uint64_t, true>(slots, kp, kp, npairs, 2 * gap * kp, stt);
           }
         }
-        write_row(p, pc.r, slots, ct, S::NC);
-        if (ct == 0) {
+        write_row(p, pc.r, slots, stt, S::NST);
+        Sel::sync();
+        for (int j = stt; j < S::INBOX; j += S::NST) inbox[j] = 0ull;  // empty slots again
+        __threadfence_block();
+        if (stt == 0) {
           p.row_theta[pc.r] = 0ull;
           atomicExch(&p.tickets[pc.r], 0u);
         }
       }
     }
-    // a clean tray for the next piece
-    Cons::sync();
-    for (int j = ct; j < kp; j += S::NC) kept[j] = 0ull;
-    if (ct == 0) {
-      st.cnt = 0;
-      st.theta = 0ull;
-      st.leader = 0;
+    // a clean tray and threshold for the next piece, then release the filters
+    Sel::sync();
+    for (int j = stt; j < kp; j += S::NST) kept[j] = 0ull;
+    tray_n = 0;
+    kept_n = 0;
+    pruned = 0;
+    theta = 0ull;
+    // skip to the next piece
+    do {
+      cursor_next(p, pcur);
+    } while (pcur.valid && pcur.pi == piece_no);
+    ++piece_no;
+    Sel::sync();
+    if (stt == 0) {
+      st.fdone = 0;
+      *reinterpret_cast<volatile uint64_t*>(&st.theta) = 0ull;
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&st.piece_gen) = piece_no;
     }
-    Cons::sync();
-    th = 0ull;
-    thf = threshold_float(th);
-  };
-
-  Cursor cur = first;
-  build_order(cur, 0);
-  for (int c = 0; cur.valid; ++c) {
-    Cursor nxt = cur;
-    cursor_next(p, nxt);
-    // one chunk ahead, so the producer never waits long
-    if (nxt.valid) build_order(nxt, (c + 1) & 1);
-    const uint32_t* pc = perm + (c & 1) * kPermChunk;
-    const int ragged_pos = st.ragged[c & 1];
-    const float* row = p.scores + int64_t(cur.pc.r) * p.row_stride;
-    const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-    const uint32_t L32 = cur.pc.L;
-    const int cs = cur.cs;
-    row_r = cur.pc.r;
-    shared_theta = cur.pc.contributors > 1;
-
-    for (int i = 0; i < cs; i += S::BPS, ++g) {
-      const uint32_t stage = g % S::NSTAGE;
-      if (!mbar_wait(&full[stage], (g / S::NSTAGE) & 1, timed_out ? 1u : kWaitLimit))
-        timed_out = true;
-      const float* src = ring + stage * S::STAGE_FLOATS;
-      // A clean stage holds BPS full blocks that were bulk-copied.
-      const bool clean = aligned && i + S::BPS <= cs &&
-                         (ragged_pos < i || ragged_pos >= i + S::BPS);
-
-      float x[S::EPT];
-      uint32_t cand = 0;  // bit e: element e may beat the threshold
-      if (clean) {
-#pragma unroll
-        for (int u = 0; u < S::F4; ++u) {
-          const float4 v = reinterpret_cast<const float4*>(src)[ct + S::NC * u];
-          x[4 * u + 0] = v.x;
-          x[4 * u + 1] = v.y;
-          x[4 * u + 2] = v.z;
-          x[4 * u + 3] = v.w;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-        // a4: one question per element.  The float compare passes a superset
-        // of the exact survivors (equal values, NaN); the word compare decides.
-#pragma unroll
-        for (int e = 0; e < S::EPT; ++e) cand |= uint32_t(!(x[e] < thf)) << e;
-      } else {
-#pragma unroll
-        for (int u = 0; u < S::F4; ++u) {
-          const int q = ct + S::NC * u;
-          const int b = q >> 8;
-          const int j0 = (q & 255) * 4;
-          const int pos = i + b;
-          uint32_t valid = 0, copied = 0, e0 = 0;
-          if (pos < cs) {
-            e0 = uint32_t(cur.cb + int32_t(pc[pos] & 1023u)) * kBlock;
-            valid = min(uint32_t(kBlock), L32 - e0);
-            copied = aligned ? (valid & ~3u) : 0u;
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t j = uint32_t(j0 + e);
-            float v = 0.f;
-            if (j < copied) v = src[b * kBlock + j];
-            else if (j < valid) v = __ldg(row + e0 + j);
-            x[4 * u + e] = v;
-            if (j < valid) cand |= uint32_t(!(v < thf)) << (4 * u + e);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-      }
-
-      bool over = false;
-      const uint32_t wcand = __reduce_or_sync(0xFFFFFFFFu, cand);
-      if (wcand) {
-        // a5: for each element slot some lane flagged, the exact word test, a
-        // ballot mask, __popc prefixes and one tray atomic per warp.
-#pragma unroll
-        for (int e = 0; e < S::EPT; ++e) {
-          if ((wcand >> e) & 1u) {
-            const bool mine = (cand >> e) & 1u;
-            bool pass = false;
-            uint64_t w = 0ull;
-            if (mine) {
-              const uint32_t bits = __float_as_uint(x[e]);
-              const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
-              saw_nan |= nan;
-              const int q = ct + S::NC * (e >> 2);
-              const uint32_t blk = uint32_t(cur.cb + int32_t(pc[i + (q >> 8)] & 1023u));
-              const uint32_t idx = blk * kBlock + uint32_t((q & 255) * 4 + (e & 3));
-              w = (uint64_t(order_key(bits)) << 32) | uint64_t(~idx);
-              pass = !nan && w > th;
-            }
-            const uint32_t pm = __ballot_sync(0xFFFFFFFFu, pass);
-            if (pm) {
-              const int n_pass = __popc(pm);
-              int base = 0;
-              if (lane == 0) {
-                base = atomicAdd(&st.cnt, n_pass);
-                over |= base + n_pass >= B;
-                admitted += uint32_t(n_pass);
-              }
-              base = __shfl_sync(0xFFFFFFFFu, base, 0);
-              if (pass) fresh[base + __popc(pm & lt_mask)] = w;
-            }
-          }
-        }
-      }
-      // Pick up a threshold raised by the row's other CTAs now and then.
-      if (shared_theta && ct == 0 && (g & 7u) == 7u) {
-        const unsigned long long gt =
-            *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[row_r]);
-        if (gt > st.theta) st.theta = gt;
-      }
-      // The tray count only grows within a stage, so it ends at or past the
-      // batch size exactly when some warp's own add took it there; deciding
-      // through the barrier keeps every consumer on the same path.
-      if (Cons::sync_or(over)) sort_batches();
-      const uint64_t nt = st.theta;
-      if (nt != th) {
-        th = nt;
-        thf = threshold_float(th);
-      }
-    }
-    if (!nxt.valid || nxt.pi != cur.pi) finish_piece(cur.pc);
-    cur = nxt;
   }
-
-  saw_nan = Cons::sync_or(saw_nan);
-  timed_out = Cons::sync_or(timed_out);
-  if (ct == 0) {
-    if (saw_nan) atomicOr(p.status, TOPK_STATUS_NAN);
-    if (timed_out) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
-  }
+  timed_out = Sel::sync_or(timed_out);
+  if (stt == 0 && timed_out) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
 }
 
 __global__ void __launch_bounds__(256)
@@ -873,7 +1127,6 @@ int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_str
   p.rows = rows;
   p.k = k;
   p.kp = kp;
-  p.batch = batch_of(kp);
   p.split = S;
   p.seg_blocks = int32_t((m_full + S - 1) / S);
   p.m_full = int32_t(m_full);
@@ -883,6 +1136,7 @@ int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_str
   p.tickets = reinterpret_cast<uint32_t*>(w + wl.tickets);
   p.survivors = reinterpret_cast<uint32_t*>(w + wl.survivors);
   p.sorts = reinterpret_cast<uint32_t*>(w + wl.sorts);
+  p.admitted = reinterpret_cast<uint32_t*>(w + wl.admitted);
   p.row_theta = reinterpret_cast<unsigned long long*>(w + wl.theta);
   p.partials = reinterpret_cast<uint64_t*>(w + wl.partials);
   p.seed_lo = uint32_t(seed);
@@ -936,7 +1190,8 @@ int topk_ws_status(void* ws, uint32_t* status_out, void* stream) {
 }
 
 int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
-                  uint32_t* survivors_out, uint32_t* sorts_out, void* stream) {
+                  uint32_t* survivors_out, uint32_t* sorts_out, uint32_t* admitted_out,
+                  void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TOPK_ERR_WS;
   if (!shape_ok(rows, n, k) || split < 0 || split > kMaxSplit) return TOPK_ERR_SHAPE;
   const int32_t S = resolve_split(rows, n, split);
@@ -945,14 +1200,14 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return TOPK_ERR_LAUNCH;
   const size_t bytes = sizeof(uint32_t) * size_t(rows);
-  if (survivors_out &&
-      cudaMemcpy(survivors_out, w + wl.survivors, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
-    return TOPK_ERR_LAUNCH;
-  if (sorts_out && cudaMemcpy(sorts_out, w + wl.sorts, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
-    return TOPK_ERR_LAUNCH;
-  if (cudaMemset(w + wl.survivors, 0, bytes) != cudaSuccess ||
-      cudaMemset(w + wl.sorts, 0, bytes) != cudaSuccess)
-    return TOPK_ERR_LAUNCH;
+  uint32_t* outs[3] = {survivors_out, sorts_out, admitted_out};
+  const size_t offs[3] = {wl.survivors, wl.sorts, wl.admitted};
+  for (int i = 0; i < 3; ++i) {
+    if (outs[i] &&
+        cudaMemcpy(outs[i], w + offs[i], bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return TOPK_ERR_LAUNCH;
+    if (cudaMemset(w + offs[i], 0, bytes) != cudaSuccess) return TOPK_ERR_LAUNCH;
+  }
   return TOPK_OK;
 }
 

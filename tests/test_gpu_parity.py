@@ -259,12 +259,13 @@ def test_survivor_bound_unsplit(layout, k):
     from sparse_attention_indexer_row_gb300 import binding as B
     w = synth.long_rows(layout, rows=8, k=k)
     gv, gi, ws = run_gpu(w.scores, w.k, split=1, return_ws=True)
-    rc, surv, sorts = B.topk_ws_stats(ws, w.rows, w.n, w.k, 1)
+    rc, surv, sorts, adm = B.topk_ws_stats(ws, w.rows, w.n, w.k, 1)
     assert rc == 0
     T = k + 2 * 1024
     bound = 1.5 * T * _harmonic(w.n // 1024)
     assert max(surv) <= bound, (max(surv), bound)
     assert min(surv) >= k
+    assert all(a >= s for a, s in zip(adm, surv))
 
 
 def test_identity_order_on_ascending_rows_admits_everything():
@@ -272,11 +273,11 @@ def test_identity_order_on_ascending_rows_admits_everything():
     from sparse_attention_indexer_row_gb300 import binding as B
     x = np.sort(np.random.default_rng(1).standard_normal((2, 1 << 18)).astype(np.float32), axis=1)
     gv, gi, ws = run_gpu(x, 512, split=1, flags=B.TOPK_FLAG_IDENTITY_ORDER, return_ws=True)
-    rc, surv, _ = B.topk_ws_stats(ws, 2, 1 << 18, 512, 1)
-    assert rc == 0 and min(surv) == 1 << 18
+    rc, surv, _, adm = B.topk_ws_stats(ws, 2, 1 << 18, 512, 1)
+    assert rc == 0 and min(adm) == 1 << 18
     gv2, gi2, ws2 = run_gpu(x, 512, split=1, return_ws=True)
-    rc, surv2, _ = B.topk_ws_stats(ws2, 2, 1 << 18, 512, 1)
-    assert max(surv2) < (1 << 18) // 10
+    rc, surv2, _, adm2 = B.topk_ws_stats(ws2, 2, 1 << 18, 512, 1)
+    assert max(adm2) < (1 << 18) // 10
     assert_bit_exact(gv, gi, gv2, gi2, "identity vs shuffled")
 
 
