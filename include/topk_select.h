@@ -51,6 +51,8 @@ extern "C" {
 #define TOPK_ERR_WS 3     /* ws NULL or not 256-byte aligned when needed */
 #define TOPK_ERR_LAUNCH 4 /* the CUDA launch reported an error */
 #define TOPK_ERR_ARG 5    /* another argument is invalid (see the function) */
+#define TOPK_ERR_NOSPACE 6 /* topk_select_noalloc: the shape needs more workspace
+                              than its built-in array holds */
 
 /* Status bits the device sets in the workspace status word (sticky until
  * read by topk_ws_status). */
@@ -170,6 +172,41 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
  */
 int topk_visit_order(int32_t m, int32_t row, int64_t first_block,
                      uint64_t seed, int32_t* order_out, void* stream);
+
+
+/*
+ * topk_select_noalloc -- topk_select for callers that cannot allocate device
+ * memory.  (An addition of this library: the pages describe no such call.)
+ *
+ * Some callers cannot call cudaMalloc where they select: code that runs while
+ * a stream is being captured into a CUDA graph and must not allocate, real-time
+ * paths that forbid allocation, or plug-ins whose host framework owns all
+ * device memory and hands them only input and output buffers.  This entry
+ * point needs no workspace argument: it uses a 16 MiB array compiled into the
+ * library (a file-scope __device__ array), which every GPU that loads the
+ * library keeps until the process exits.  It calls no cudaMalloc or cudaFree.
+ *
+ *   Arguments as topk_select, without `ws`.  `status_or_null`: optional device
+ *   uint32 that receives this call's status word (TOPK_STATUS_* bits).
+ *
+ *   Limit: shapes whose topk_ws_bytes(rows, n, k) exceeds 16 MiB return
+ *   TOPK_ERR_NOSPACE (for example, k = 2048 on fewer than 152 rows needs about
+ *   8.4 MiB; one CTA per row needs about 20 bytes per row).
+ *
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before capturing a stream into a
+ *   graph.  Every call shares the one array: the call clears the parts that
+ *   must start at zero (status, tickets, counters) on `stream`, and two calls
+ *   that may overlap on the GPU -- on different streams, or from different
+ *   host threads -- race on it and must be serialised by the caller.
+ *
+ * Returns TOPK_OK, TOPK_ERR_SHAPE, TOPK_ERR_NULL, TOPK_ERR_NOSPACE or
+ * TOPK_ERR_LAUNCH.
+ */
+int topk_select_noalloc(const float* scores, int32_t rows, int64_t n,
+                        int64_t row_stride, const int32_t* lengths_or_null,
+                        int32_t k, float* out_vals, int32_t* out_idx,
+                        uint32_t* status_or_null, void* stream);
 
 #ifdef __cplusplus
 }

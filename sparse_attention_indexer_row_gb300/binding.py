@@ -20,6 +20,7 @@ TOPK_ERR_NULL = 2
 TOPK_ERR_WS = 3
 TOPK_ERR_LAUNCH = 4
 TOPK_ERR_ARG = 5
+TOPK_ERR_NOSPACE = 6
 TOPK_STATUS_NAN = 1
 TOPK_STATUS_BAD_LENGTH = 2
 TOPK_STATUS_TIMEOUT = 4
@@ -39,6 +40,7 @@ SIGNATURES = {
     "topk_ws_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _P]),
     "topk_ws_stats": (ctypes.c_int, [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P]),
     "topk_visit_order": (ctypes.c_int, [_I32, _I32, _I64, _U64, _P, _P]),
+    "topk_select_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _P, _P, _P, _P]),
 }
 
 
@@ -120,6 +122,15 @@ def topk_ws_stats(ws, rows, n, k, split=0, stream=None):
 def topk_visit_order(m, row, first_block, seed, order_out, stream=None) -> int:
     return int(LIB.topk_visit_order(m, row, first_block, seed & 0xFFFFFFFFFFFFFFFF,
                                     _ptr(order_out), _stream(stream)))
+
+
+def topk_select_noalloc(scores, rows, n, row_stride, lengths_or_null, k, out_vals, out_idx,
+                        status_or_null=None, stream=None) -> int:
+    """topk_select without a workspace argument, for callers that cannot
+    allocate device memory (the library's built-in 16 MiB array is used)."""
+    return int(LIB.topk_select_noalloc(_ptr(scores), rows, n, row_stride, _ptr(lengths_or_null),
+                                       k, _ptr(out_vals), _ptr(out_idx), _ptr(status_or_null),
+                                       _stream(stream)))
 
 
 class TopK:

@@ -1084,6 +1084,79 @@ int32_t resolve_split(int32_t rows, int64_t n, int32_t split) {
 
 using namespace topk;
 
+// ---------------------------------------------------------------------------
+// Workspace for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at the point where they select: code
+// running inside a CUDA-graph capture that must not allocate, allocation-free
+// real-time paths, plug-ins whose host framework owns every allocation and
+// hands out only input and output buffers.  For them topk_select_noalloc uses
+// this file-scope device array as its workspace.  Every GPU that loads this
+// library keeps the array (kNoAllocWsBytes) until the process exits.  In host
+// code `g_noalloc_ws` names a host-side stand-in, not device memory: its
+// device address is looked up once per device with cudaGetSymbolAddress.
+constexpr size_t kNoAllocWsBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocWsBytes];
+
+namespace {
+
+struct NoAllocSlot {
+  std::atomic<int> ready{0};
+  void* ptr = nullptr;
+};
+NoAllocSlot g_noalloc_slots[64];
+
+// Device address of the static workspace on the current device (set up on
+// the first call per device, with that device current).
+cudaError_t noalloc_ws_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  NoAllocSlot& slot = g_noalloc_slots[dev];
+  if (!slot.ready.load()) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
+    if (e != cudaSuccess) return e;
+    slot.ptr = ptr;
+    slot.ready.store(1);
+  }
+  *out = slot.ptr;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+int topk_select_noalloc(const float* scores, int32_t rows, int64_t n, int64_t row_stride,
+                        const int32_t* lengths_or_null, int32_t k, float* out_vals,
+                        int32_t* out_idx, uint32_t* status_or_null, void* stream) {
+  if (!shape_ok(rows, n, k) || row_stride < n) return TOPK_ERR_SHAPE;
+  if (rows == 0) return TOPK_OK;
+  const size_t need = topk_ws_bytes_ex(rows, n, k, 0);
+  if (need == 0) return TOPK_ERR_SHAPE;
+  if (need > kNoAllocWsBytes) return TOPK_ERR_NOSPACE;
+  void* ws = nullptr;
+  if (noalloc_ws_address(&ws) != cudaSuccess) return TOPK_ERR_LAUNCH;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the status word, tickets,
+  // counters and row thresholds (everything before the partial lists) must
+  // start at zero.
+  const WsLayout wl = ws_layout(rows, next_pow2(k), partial_slots(rows, 0, resolve_split(rows, n, 0)));
+  if (cudaMemsetAsync(ws, 0, wl.partials, st) != cudaSuccess) return TOPK_ERR_LAUNCH;
+  const int rc = topk_select(scores, rows, n, row_stride, lengths_or_null, k, out_vals, out_idx,
+                             ws, stream);
+  if (rc != TOPK_OK) return rc;
+  if (status_or_null &&
+      cudaMemcpyAsync(status_or_null, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) !=
+          cudaSuccess)
+    return TOPK_ERR_LAUNCH;
+  return TOPK_OK;
+}
+
+}  // extern "C"
+
 extern "C" {
 
 int32_t topk_split_plan(int32_t rows, int64_t n) {
