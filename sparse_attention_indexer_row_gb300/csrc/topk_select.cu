@@ -76,6 +76,7 @@ constexpr int kPermChunk = 1024;      // blocks shuffled together
 constexpr int kTrayMark = 2048;       // tray words that trigger the tray sort
 constexpr int kPruneStep = 512;       // new tray words that trigger a prune
 constexpr int kSelectSlack = 256;     // extra words a pruned tray may keep
+constexpr int kWarmElems = 8192;      // warm start: the first 32 KB of each piece
 constexpr int kMaxSplit = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait gives up
 
@@ -543,6 +544,22 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
     bool saw_nan = false, timed_out = false;
     int gen = 0;
     uint32_t g = 0;
+    // Wait until the selectors have released piece `piece` (with its warm-start
+    // threshold in place), then pick up that threshold.
+    auto gate = [&](int piece) {
+      uint32_t it = timed_out ? kWaitLimit : 0u;
+      while (*reinterpret_cast<volatile int*>(&st.piece_gen) < piece + 1) {
+        if (++it > kWaitLimit) {
+          timed_out = true;
+          break;
+        }
+        __nanosleep(128);
+      }
+      __syncwarp();
+      th = *reinterpret_cast<volatile uint64_t*>(&st.theta);
+      thf = threshold_float(th);
+    };
+    gate(0);
     Cursor cur = first;
     for (int c = 0; cur.valid; ++c) {
       const float* row = p.scores + int64_t(cur.pc.r) * p.row_stride;
@@ -578,12 +595,65 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
             x[4 * u + 2] = v.z;
             x[4 * u + 3] = v.w;
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[stage]);
           // One question per element.  The float compare passes a superset of
           // the exact survivors (equal values, NaN); the word compare decides.
 #pragma unroll
           for (int e = 0; e < S::EPT; ++e) cand |= uint32_t(!(x[e] < thf)) << e;
+          if (__any_sync(0xFFFFFFFFu, cand != 0u)) {
+            // Each lane walks only its own flagged elements (re-read from the
+            // stage, which is not released yet): exact word test, then a warp
+            // prefix of the per-lane pass counts from five ballot masks and
+            // __popc, one inbox reservation, and the writes.
+            auto word_at = [&](int e, bool& nan) -> uint64_t {
+              const int q = ft + S::NFT * (e >> 2);
+              const uint32_t bits = __float_as_uint(src[q * 4 + (e & 3)]);
+              nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+              const uint32_t idx = desc[stage * S::BPS + (q >> 8)] + uint32_t((q & 255) * 4 + (e & 3));
+              return (uint64_t(order_key(bits)) << 32) | uint64_t(~idx);
+            };
+            uint32_t passm = 0;
+            for (uint32_t m = cand; m; m &= m - 1u) {
+              const int e = __ffs(m) - 1;
+              bool nan;
+              const uint64_t w = word_at(e, nan);
+              saw_nan |= nan;
+              if (!nan && w > th) passm |= 1u << e;
+            }
+            const uint32_t np = __popc(passm);
+            uint32_t off = 0, total = 0;
+#pragma unroll
+            for (int b = 0; b < 6; ++b) {
+              const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (np >> b) & 1u);
+              off += uint32_t(__popc(bal & lt_mask)) << b;
+              total += uint32_t(__popc(bal)) << b;
+            }
+            if (total) {
+              uint32_t pos = 0;
+              if (lane == 0) {
+                pos = atomicAdd(&st.tail, total);
+                admitted += total;
+                // wait for room: the selectors free slots by advancing head
+                uint32_t it = timed_out ? kWaitLimit : 0u;
+                while (pos + total - *reinterpret_cast<volatile uint32_t*>(&st.head) >
+                       uint32_t(S::INBOX)) {
+                  if (++it > kWaitLimit) {
+                    timed_out = true;
+                    break;
+                  }
+                  __nanosleep(64);
+                }
+              }
+              pos = __shfl_sync(0xFFFFFFFFu, pos, 0) + off;
+              for (uint32_t m = passm; m; m &= m - 1u) {
+                bool nan;
+                const uint64_t w = word_at(__ffs(m) - 1, nan);
+                reinterpret_cast<volatile uint64_t*>(inbox)[pos & (S::INBOX - 1)] = w;
+                ++pos;
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[stage]);
         } else {
 #pragma unroll
           for (int u = 0; u < S::F4; ++u) {
@@ -610,11 +680,12 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
           if (lane == 0) mbar_arrive(&empty[stage]);
         }
 
-        const uint32_t wcand = __reduce_or_sync(0xFFFFFFFFu, cand);
+        const uint32_t wcand = clean ? 0u : __reduce_or_sync(0xFFFFFFFFu, cand);
         if (wcand) {
-          // For each element slot some lane flagged: the exact word test and a
-          // ballot mask; then one inbox reservation for the warp and the writes
-          // at __popc prefix offsets.
+          // Stages with ragged or unaligned blocks (values partly read from
+          // global memory): for each element slot some lane flagged, the exact
+          // word test and a ballot mask; then one inbox reservation for the
+          // warp and the writes at __popc prefix offsets.
           uint32_t pm[S::EPT];
           int total = 0;
 #pragma unroll
@@ -671,7 +742,7 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
       cursor_next(p, nxt);
       if (!nxt.valid || nxt.pi != cur.pi) {
         // end of a piece: report, then wait until the selectors have finished
-        // it before filtering the next piece with a fresh threshold
+        // it and set the next piece's warm-start threshold
         __syncwarp();
         if (lane == 0) {
           if (admitted) atomicAdd(&p.admitted[cur.pc.r], admitted);
@@ -680,19 +751,7 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
         }
         admitted = 0;
         ++gen;
-        if (nxt.valid) {
-          uint32_t it = timed_out ? kWaitLimit : 0u;
-          while (*reinterpret_cast<volatile int*>(&st.piece_gen) < gen) {
-            if (++it > kWaitLimit) {
-              timed_out = true;
-              break;
-            }
-            __nanosleep(128);
-          }
-          __syncwarp();
-          th = *reinterpret_cast<volatile uint64_t*>(&st.theta);
-          thf = threshold_float(th);
-        }
+        if (nxt.valid) gate(gen);
       }
       cur = nxt;
     }
@@ -878,10 +937,114 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
     if (stt == 0) *reinterpret_cast<volatile uint32_t*>(&st.head) = head;
   };
 
+  // Warm start: before the filters see a piece, take a threshold from its
+  // first 32 KB (the first stages of its first chunk, read where they sit in
+  // the ring -- the filters are held back, so the producer cannot reuse those
+  // stages yet).  A key prefix T with at least k of those elements at or above
+  // it bounds the piece's k-th largest from below, so every filter starts with
+  // a working threshold instead of -inf.
+  auto warm_start = [&](const Cursor& cu, uint32_t g0, int chunk, const Piece& pc) {
+    // The producer needs this chunk's visiting order before it can fill the
+    // stages waited on below.  It has finished every chunk before this one
+    // (the filters completed them), so the order's buffer is free.
+    if (bcur.valid && built <= chunk) build_next();
+    const int nst = min((kWarmElems + S::STAGE_FLOATS - 1) / S::STAGE_FLOATS,
+                        (cu.cs + S::BPS - 1) / S::BPS);
+    for (int sidx = 0; sidx < nst; ++sidx) {
+      const uint32_t gs = g0 + uint32_t(sidx);
+      if (!mbar_wait(&full[gs % S::NSTAGE], (gs / S::NSTAGE) & 1, timed_out ? 1u : kWaitLimit))
+        timed_out = true;
+    }
+    const float* row = p.scores + int64_t(pc.r) * p.row_stride;
+    const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    // key of sample element j, or 0 for an empty slot or NaN (no valid key is 0)
+    auto sample_key = [&](int j) -> uint32_t {
+      const int sidx = j / S::STAGE_FLOATS;
+      const int e = j - sidx * S::STAGE_FLOATS;
+      const uint32_t stage = (g0 + uint32_t(sidx)) % S::NSTAGE;
+      const uint32_t e0 = desc[stage * S::BPS + (e >> 10)];
+      if (e0 == kNoBlock) return 0u;
+      const uint32_t jj = uint32_t(e & (kBlock - 1));
+      const uint32_t valid = min(uint32_t(kBlock), pc.L - e0);
+      if (jj >= valid) return 0u;
+      const float x = (aligned && jj < (valid & ~3u)) ? ring[stage * S::STAGE_FLOATS + e]
+                                                      : __ldg(row + e0 + jj);
+      const uint32_t bits = __float_as_uint(x);
+      return (bits & 0x7FFFFFFFu) > 0x7F800000u ? 0u : order_key(bits);
+    };
+    const int total = nst * S::STAGE_FLOATS;
+    if (stt == 0) st.cnt2 = 0;
+    Sel::sync();
+    int mine = 0;
+    for (int j = stt; j < total; j += S::NST) mine += sample_key(j) != 0u;
+    atomicAdd(&st.cnt2, mine);
+    Sel::sync();
+    if (st.cnt2 < k) return;  // too few elements to bound anything
+    const int slack = kp >= kTrayMark ? 0 : kSelectSlack;
+    uint32_t prefix = 0, need = uint32_t(k), greater = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      const uint32_t hmask = pass == 0 ? 0u : (~0u << (shift + 8));
+      for (int b = stt; b < 256; b += S::NST) hist[b] = 0u;
+      Sel::sync();
+      for (int j = stt; j < total; j += S::NST) {
+        const uint32_t key = sample_key(j);
+        if (key != 0u && (key & hmask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFFu], 1u);
+      }
+      Sel::sync();
+      if (swarp == 0) {
+        uint32_t cnt8[8], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          cnt8[q] = hist[255 - 8 * lane - q];
+          sum += cnt8[q];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+          if (lane >= d) incl += o;
+        }
+        const uint32_t excl = incl - sum;
+        if (excl < need && incl >= need) {
+          uint32_t acc = excl;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (acc < need && acc + cnt8[q] >= need) {
+              st.sel_b = 255 - 8 * lane - q;
+              st.sel_above = int(acc);
+              st.sel_binc = int(cnt8[q]);
+            }
+            acc += cnt8[q];
+          }
+        }
+      }
+      Sel::sync();
+      const uint32_t b = uint32_t(st.sel_b);
+      const uint32_t above = uint32_t(st.sel_above), binc = uint32_t(st.sel_binc);
+      Sel::sync();
+      prefix |= b << shift;
+      greater += above;
+      need -= above;
+      if (greater + binc <= uint32_t(k + slack) || pass == 3) break;
+    }
+    // words w > (prefix << 32) - 1 are exactly the words whose key is >= prefix;
+    // a zero prefix bounds nothing
+    if (prefix) raise_theta((uint64_t(prefix) << 32) - 1ull, pc);
+  };
+
   Cursor pcur = first;  // the piece being selected
   int piece_no = 0;
+  uint32_t g_sel = 0;   // ring stage index where the piece starts
+  int pchunk = 0;       // chunk index where the piece starts
   while (pcur.valid) {
     const Piece pc = pcur.pc;
+    warm_start(pcur, g_sel, pchunk, pc);
+    Sel::sync();
+    if (stt == 0) {
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&st.piece_gen) = piece_no + 1;  // release the filters
+    }
     uint32_t idle = 0;
     for (;;) {
       // build the next visiting order once the producer no longer reads its buffer
@@ -1015,16 +1178,17 @@ __global__ void __launch_bounds__(S::NTHREADS, S::MIN_BLOCKS) topk_select_kernel
     theta = 0ull;
     // skip to the next piece
     do {
+      g_sel += uint32_t((pcur.cs + S::BPS - 1) / S::BPS);
       cursor_next(p, pcur);
+      ++pchunk;
     } while (pcur.valid && pcur.pi == piece_no);
     ++piece_no;
     Sel::sync();
     if (stt == 0) {
       st.fdone = 0;
       *reinterpret_cast<volatile uint64_t*>(&st.theta) = 0ull;
-      __threadfence_block();
-      *reinterpret_cast<volatile int*>(&st.piece_gen) = piece_no;
     }
+    Sel::sync();
   }
   timed_out = Sel::sync_or(timed_out);
   if (stt == 0 && timed_out) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
