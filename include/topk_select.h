@@ -17,8 +17,9 @@
  * status word (TOPK_STATUS_NAN) and is left out of the selection.
  *
  * Method: one threshold per row that only rises, a shared-memory candidate
- * tray, 1024-element blocks streamed once in a seeded shuffled order, a
- * bitonic sort that runs on the tray only, and for short batches a split of
+ * tray, 1024-element blocks streamed once (in units of eight consecutive
+ * blocks visited in a seeded shuffled order), a bitonic sort that runs on the
+ * tray only, and for short batches a split of
  * each row over several CTAs whose local winners a ticket-elected leader
  * merges (video transcript 3:18-5:45).
  *
@@ -62,7 +63,7 @@ extern "C" {
                                      affected rows' outputs are unspecified */
 
 /* Flags for topk_select_ex. */
-#define TOPK_FLAG_IDENTITY_ORDER 1u /* visit blocks in address order instead of
+#define TOPK_FLAG_IDENTITY_ORDER 1u /* visit units in address order instead of
                                        the shuffled order (diagnostic: the
                                        result is the same, the speed is not) */
 
@@ -164,13 +165,19 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
 
 /*
  * topk_visit_order -- diagnostic: writes to device int32 order_out[m] the
- * order in which a CTA visits the m <= 1024 blocks of one permutation chunk,
- * given the chunk's row, its first block index in the row and the seed: the
- * blocks sorted by (Philox4x32-10(counter = (first_block + j, row, 0, 0),
- * key = seed) word 0 with its low 10 bits cleared, j).  Enqueued on `stream`.
- * Returns TOPK_ERR_ARG for m outside [1, 1024] or a NULL order_out.
+ * order in which a CTA visits the m <= 256 units of one permutation chunk.
+ * A unit is 8 consecutive 1024-element blocks (8192 elements, 32 KB; a row's
+ * last unit may be shorter); unit u of a row starts at element 8192 * u.
+ * Given the chunk's row, its first unit index in the row and the seed, the
+ * order is the chunk's units sorted by (Philox4x32-10(counter =
+ * (first_unit + j, row, 0, 0), key = seed) word 0 with its low 8 bits
+ * cleared, j).  (When a row's short last unit would come first in its piece,
+ * the kernel swaps the first two entries, so that the warm start reads a full
+ * unit; this call reports the order before that swap.)  Enqueued on `stream`.
+ * Returns TOPK_ERR_ARG for m outside [1, 256], a negative first_unit or a
+ * NULL order_out.
  */
-int topk_visit_order(int32_t m, int32_t row, int64_t first_block,
+int topk_visit_order(int32_t m, int32_t row, int64_t first_unit,
                      uint64_t seed, int32_t* order_out, void* stream);
 
 

@@ -119,8 +119,8 @@ def topk_ws_stats(ws, rows, n, k, split=0, stream=None):
     return (rc, *[list(a)[:rows] for a in arrs])
 
 
-def topk_visit_order(m, row, first_block, seed, order_out, stream=None) -> int:
-    return int(LIB.topk_visit_order(m, row, first_block, seed & 0xFFFFFFFFFFFFFFFF,
+def topk_visit_order(m, row, first_unit, seed, order_out, stream=None) -> int:
+    return int(LIB.topk_visit_order(m, row, first_unit, seed & 0xFFFFFFFFFFFFFFFF,
                                     _ptr(order_out), _stream(stream)))
 
 

@@ -70,5 +70,5 @@ def test_host_validation_returns_codes(B):
     assert B.topk_select_ex(4096, 2, 100, 100, None, 5, 4096, 4096, 4096, None, 65) == \
         B.TOPK_ERR_SHAPE
     assert B.topk_visit_order(0, 0, 0, 1, 4096) == B.TOPK_ERR_ARG
-    assert B.topk_visit_order(1025, 0, 0, 1, 4096) == B.TOPK_ERR_ARG
+    assert B.topk_visit_order(257, 0, 0, 1, 4096) == B.TOPK_ERR_ARG
     assert B.topk_ws_status(0)[0] == B.TOPK_ERR_WS

@@ -117,16 +117,17 @@ def test_misaligned_and_padded_rows(stride_pad):
 
 
 def test_multi_chunk_segments():
-    """Segments longer than one 1024-block shuffle chunk, in both CTA shapes."""
+    """Pieces longer than one shuffle chunk (256 units of 8192 elements), split
+    and unsplit, and many variable-length rows dealt round-robin."""
     rng = np.random.default_rng(31)
     x = rng.standard_normal((2, 2_500_003)).astype(np.float32)
-    gv, gi = run_gpu(x, 512, split=1)                 # few rows: the wide CTA
+    gv, gi = run_gpu(x, 512, split=1)                 # two 2-chunk pieces
     ov, oi = oracle_rows(x, 512)
     assert_bit_exact(gv, gi, ov, oi, "2 x 2.5M unsplit")
     y = rng.standard_normal((160, 1_100_005)).astype(np.float32)
     lengths = rng.integers(0, 1_100_006, size=160).astype(np.int32)
     lengths[:4] = [1_100_005, 1_048_577, 1_048_576, 0]
-    gv, gi = run_gpu(y, 1000, lengths=lengths)        # many rows: the narrow CTA
+    gv, gi = run_gpu(y, 1000, lengths=lengths)        # many rows, one item each
     ov, oi = oracle_rows(y, 1000, lengths=lengths)
     assert_bit_exact(gv, gi, ov, oi, "160 x 1.1M")
 
@@ -278,21 +279,21 @@ def test_identity_order_on_ascending_rows_admits_everything():
     assert rc == 0 and min(adm) >= (1 << 18) - 8192
     gv2, gi2, ws2 = run_gpu(x, 512, split=1, return_ws=True)
     rc, surv2, _, adm2 = B.topk_ws_stats(ws2, 2, 1 << 18, 512, 1)
-    assert max(adm2) < (1 << 18) // 10
+    assert max(adm2) < (1 << 18) // 4
     assert_bit_exact(gv, gi, gv2, gi2, "identity vs shuffled")
 
 
 def test_visit_order_matches_philox():
     from sparse_attention_indexer_row_gb300 import binding as B
     from tests.philox_ref import philox4x32_10
-    for m, row, first, seed in [(1024, 3, 0, 0x1234), (205, 17, 410, 0xDEADBEEFCAFEF00D), (1, 0, 5, 7)]:
+    for m, row, first, seed in [(256, 3, 0, 0x1234), (205, 17, 410, 0xDEADBEEFCAFEF00D), (1, 0, 5, 7)]:
         out = torch.empty(m, dtype=torch.int32, device="cuda")
         assert B.topk_visit_order(m, row, first, seed, out) == 0
         got = out.cpu().numpy()
         keys = []
         for j in range(m):
             r = philox4x32_10((first + j, row, 0, 0), (seed & 0xFFFFFFFF, seed >> 32))
-            keys.append(((r[0] & ~1023) & 0xFFFFFFFF) | j)
+            keys.append(((r[0] & ~255) & 0xFFFFFFFF) | j)
         want = np.argsort(np.array(keys, dtype=np.uint64), kind="stable")
         assert np.array_equal(got, want)
         assert np.array_equal(np.sort(got), np.arange(m))
