@@ -118,9 +118,13 @@ constexpr int kInbox = 2048;                     // words per inbox (two inboxes
 constexpr int kTray = 3072;                      // tray words
 constexpr int kTable = 16;                       // piece descriptors in flight
 // Inbox words the selectors move per step.  A take must never reach a slot
-// reserved by a filter warp that is itself waiting for room, so it stays at
-// least one warp-stage reservation (32 * kEPT words) short of the inbox size.
-constexpr int kTakeMax = (kInbox - 32 * kEPT) < 1024 ? (kInbox - 32 * kEPT) : 1024;
+// reserved by a filter lane that is itself waiting for room, so it stays at
+// least one lane-stage reservation (kEPT words) short of the inbox size.
+constexpr int kTakeMax = (kInbox - kEPT) < 1024 ? (kInbox - kEPT) : 1024;
+// Smallest batch the selectors take while the piece's filters are still
+// running (a prune needs kPruneStep new words anyway); polling for less only
+// takes issue slots from the filter warps.
+constexpr int kTakeMin = 256;
 static_assert(kEPT == 32, "one candidate bit per element of a thread's stage share");
 static_assert((kInbox & (kInbox - 1)) == 0, "inbox ring size is a power of two");
 static_assert(kTakeMax >= 256, "inbox leaves room for a take");
@@ -466,10 +470,15 @@ __device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint3
 #pragma unroll 1
   for (int b = 31; b >= 16; --b) {
     const uint32_t t = T | (1u << b);
-    uint32_t c = 0;
+    uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
 #pragma unroll
-    for (int e = 0; e < kEPT; ++e) c += key[e] >= t ? 1u : 0u;
-    if (__reduce_add_sync(0xFFFFFFFFu, c) >= uint32_t(m)) T = t;
+    for (int e = 0; e < kEPT; e += 4) {
+      c0 += key[e + 0] >= t ? 1u : 0u;
+      c1 += key[e + 1] >= t ? 1u : 0u;
+      c2 += key[e + 2] >= t ? 1u : 0u;
+      c3 += key[e + 3] >= t ? 1u : 0u;
+    }
+    if (__reduce_add_sync(0xFFFFFFFFu, (c0 + c1) + (c2 + c3)) >= uint32_t(m)) T = t;
   }
   return T;
 }
@@ -647,7 +656,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   // ---------------- filter warps: a4 + a5 and the warm start ----------------
   if (warp < kNF) {
     const int ft = tid;  // 0 .. kNFT-1
-    const uint32_t lt_mask = (1u << lane) - 1u;
     const int m_warm = (k + kNF - 1) / kNF;
     uint64_t th = 0ull;
     float thf = threshold_float(th);
@@ -770,60 +778,91 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         }
         thf = threshold_float(th);
       }
-      uint32_t cand = 0;  // bit e: element e may beat the threshold
+      // Most stages have no element past the threshold: one chained float
+      // test first (a superset: it also passes NaN, ties and padding), the
+      // per-element mask only when some lane needs it.
+      // (four independent chains keep the test short in latency)
+      bool m0 = false, m1 = false, m2 = false, m3 = false;
 #pragma unroll
-      for (int e = 0; e < kEPT; ++e) cand |= uint32_t(!(x[e] < thf)) << e;
-      cand &= valid;
-      if (__any_sync(0xFFFFFFFFu, cand != 0u)) {
-        // Each lane walks only its own flagged elements (re-read from the
-        // stage, which is not released yet): exact word test, then a warp
-        // prefix of the per-lane pass counts from six ballot masks and
-        // __popc, one inbox reservation, and the writes.
-        auto word_at = [&](int e, bool& nan) -> uint64_t {
+      for (int u = 0; u < kF4; ++u) {
+        m0 |= !(x[4 * u + 0] < thf);
+        m1 |= !(x[4 * u + 1] < thf);
+        m2 |= !(x[4 * u + 2] < thf);
+        m3 |= !(x[4 * u + 3] < thf);
+      }
+      if (__any_sync(0xFFFFFFFFu, (m0 | m1) | (m2 | m3))) {
+        uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;  // bit e: element e may beat the threshold
+#pragma unroll
+        for (int u = 0; u < kF4; ++u) {
+          c0 |= uint32_t(!(x[4 * u + 0] < thf)) << (4 * u + 0);
+          c1 |= uint32_t(!(x[4 * u + 1] < thf)) << (4 * u + 1);
+          c2 |= uint32_t(!(x[4 * u + 2] < thf)) << (4 * u + 2);
+          c3 |= uint32_t(!(x[4 * u + 3] < thf)) << (4 * u + 3);
+        }
+        const uint32_t cand = ((c0 | c1) | (c2 | c3)) & valid;
+        // Exact word test of the flagged elements.  On a full stage each lane
+        // walks only its own set bits, re-reading them from the stage (not
+        // released yet); a ragged stage has its values in registers already
+        // and takes a fixed walk over all of them.  Then each lane with
+        // survivors reserves its own run of inbox slots (one shared-memory
+        // atomicAdd) and writes them.
+        const bool clean = copied == uint32_t(kUnit);
+        auto word_of = [&](uint32_t bits, int e) -> uint64_t {
           const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
-          const float v = pos < copied ? src[pos] : __ldg(row + e0 + pos);
-          const uint32_t bits = __float_as_uint(v);
-          nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
           return (uint64_t(order_key(bits)) << 32) | uint64_t(~(e0 + pos));
         };
+        auto smem_bits = [&](int e) -> uint32_t {
+          return __float_as_uint(src[4 * (ft + kNFT * (e >> 2)) + (e & 3)]);
+        };
         uint32_t passm = 0;
-        for (uint32_t mm = cand; mm; mm &= mm - 1u) {
-          const int e = __ffs(mm) - 1;
-          bool nan;
-          const uint64_t w = word_at(e, nan);
-          saw_nan |= nan;
-          if (!nan && w > th) passm |= 1u << e;
-        }
-        const uint32_t np = __popc(passm);
-        uint32_t off = 0, total = 0;
+        if (clean) {
+          for (uint32_t mm = cand; mm; mm &= mm - 1u) {
+            const int e = __ffs(mm) - 1;
+            const uint32_t bits = smem_bits(e);
+            const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+            saw_nan |= nan;
+            if (!nan && word_of(bits, e) > th) passm |= 1u << e;
+          }
+        } else {
 #pragma unroll
-        for (int b = 0; b < 6; ++b) {
-          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (np >> b) & 1u);
-          off += uint32_t(__popc(bal & lt_mask)) << b;
-          total += uint32_t(__popc(bal)) << b;
-        }
-        if (total) {
-          uint32_t pos = 0;
-          if (lane == 0) {
-            pos = atomicAdd(&st.tail[par], total);
-            admitted += total;
-            // wait for room: the selectors free slots by advancing head
-            uint32_t it = timed_out ? kWaitLimit : 0u;
-            while (pos + total - *reinterpret_cast<volatile uint32_t*>(&st.head[par]) >
-                   uint32_t(kInbox)) {
-              if (++it > kWaitLimit) {
-                timed_out = true;
-                break;
-              }
-              __nanosleep(64);
+          for (int e = 0; e < kEPT; ++e) {
+            if ((cand >> e) & 1u) {
+              const uint32_t bits = __float_as_uint(x[e]);
+              const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+              saw_nan |= nan;
+              if (!nan && word_of(bits, e) > th) passm |= 1u << e;
             }
           }
-          pos = __shfl_sync(0xFFFFFFFFu, pos, 0) + off;
+        }
+        const uint32_t np = __popc(passm);
+        if (np) {
+          uint32_t pos = atomicAdd(&st.tail[par], np);
+          admitted += np;
+          // wait for room: the selectors free slots by advancing head
+          uint32_t it = timed_out ? kWaitLimit : 0u;
+          while (pos + np - *reinterpret_cast<volatile uint32_t*>(&st.head[par]) >
+                 uint32_t(kInbox)) {
+            if (++it > kWaitLimit) {
+              timed_out = true;
+              break;
+            }
+            __nanosleep(64);
+          }
           volatile uint64_t* ib = inboxes[par];
-          for (uint32_t mm = passm; mm; mm &= mm - 1u) {
-            bool nan;
-            ib[pos & (kInbox - 1)] = word_at(__ffs(mm) - 1, nan);
-            ++pos;
+          if (clean) {
+            for (uint32_t mm = passm; mm; mm &= mm - 1u) {
+              const int e = __ffs(mm) - 1;
+              ib[pos & (kInbox - 1)] = word_of(smem_bits(e), e);
+              ++pos;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < kEPT; ++e) {
+              if ((passm >> e) & 1u) {
+                ib[pos & (kInbox - 1)] = word_of(__float_as_uint(x[e]), e);
+                ++pos;
+              }
+            }
           }
         }
       }
@@ -831,6 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (lane == 0) mbar_arrive(&empty[stage]);
       if (d.tag & kLast) {
         __syncwarp();
+        admitted = __reduce_add_sync(0xFFFFFFFFu, admitted);
         if (lane == 0) {
           if (admitted) atomicAdd(&p.admitted[r], admitted);
           __threadfence_block();
@@ -885,8 +925,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   // threshold rises to T.  With `sort` (the tray has passed its mark, or the
   // piece is done) the rest are bitonic-sorted and merged into the kept
   // list, whose k-th word becomes the threshold, and the tray is emptied.
-  auto process_tray = [&](bool sort, const Piece& pc) {
-    const int slack = kp >= kTrayMark ? 0 : kSelectSlack;
+  auto process_tray = [&](bool sort, bool final, const Piece& pc) {
+    // at the end of a piece the select is exact (no slack): at most kp words
+    // are left to sort
+    const int slack = (final || kp >= kTrayMark) ? 0 : kSelectSlack;
     uint64_t T = 0ull;
     if (kept_n + tray_n > kp + slack) {
       uint64_t prefix = 0ull;
@@ -896,9 +938,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         const uint64_t hmask = pass == 0 ? 0ull : (~0ull << (shift + 8));
         for (int b = stt; b < 256; b += kNST) hist[b] = 0u;
         Sel::sync();
-        for (int j = stt; j < kp + tray_n; j += kNST) {
-          const uint64_t w = j < kp ? kept[j] : tray[j - kp];
-          if (w != 0ull && (w & hmask) == prefix) atomicAdd(&hist[(w >> shift) & 0xFFu], 1u);
+        // the kept list holds its kept_n real words first
+        const int nw = kept_n + tray_n;
+        for (int j = stt; j < nw; j += kNST) {
+          const uint64_t w = j < kept_n ? kept[j] : tray[j - kept_n];
+          if ((w & hmask) == prefix) atomicAdd(&hist[uint32_t(w >> shift) & 0xFFu], 1u);
         }
         Sel::sync();
         if (swarp == 0) {
@@ -980,7 +1024,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     for (int t = r + stt; t < P; t += kNST) tray[t] = 0ull;
     Sel::sync();
     bitonic_network<Sel, uint64_t, true>(tray, P, 2, 1, 0, stt);
-    merge_into_kept<Sel>(kept, tray, P, kp, stt);
+    if (kept_n == 0) {
+      // nothing kept yet: the sorted tray is the list
+      for (int q = stt; q < kp; q += kNST) kept[q] = q < P ? tray[q] : 0ull;
+      Sel::sync();
+    } else {
+      merge_into_kept<Sel>(kept, tray, P, kp, stt);
+    }
     ++nsorts;
     nsorted += uint32_t(r);
     kept_n = min(kp, kept_n + r);
@@ -1046,23 +1096,36 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     par = j & 1;
     const int fd_target = kNF * (j / 2 + 1);
 
-    uint32_t idle = 0;
     for (;;) {
-      // what is waiting: read the finished-filter count before the tail, so a
-      // full count means the tail is final
+      // One lane polls until there is a batch to take or the piece is done;
+      // the rest of the team waits at the barrier.  The finished-filter count
+      // is read before the tail, so a full count means the tail is final.
       if (stt == 0) {
-        const int fd = *reinterpret_cast<volatile int*>(&st.fdone[par]);
-        const uint32_t tail = *reinterpret_cast<volatile uint32_t*>(&st.tail[par]);
-        const uint32_t avail = tail - head[par];
-        int n = int(min(avail, uint32_t(kTray - tray_n)));
-        if (n > kTakeMax) n = kTakeMax;
-        st.sel_n = n;
-        st.sel_done = (fd >= fd_target && avail == 0) ? 1 : 0;
-        if (pc.contributors > 1) {
-          const unsigned long long gt =
-              *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[pc.r]);
-          if (gt > theta) atomicMax(&st.theta[par], gt);
+        uint32_t it = timed_out ? kWaitLimit : 0u;
+        int n = 0, done = 0;
+        for (;;) {
+          const int fd = *reinterpret_cast<volatile int*>(&st.fdone[par]);
+          const uint32_t tail = *reinterpret_cast<volatile uint32_t*>(&st.tail[par]);
+          const uint32_t avail = tail - head[par];
+          n = int(min(avail, uint32_t(kTray - tray_n)));
+          if (n > kTakeMax) n = kTakeMax;
+          if (fd < fd_target && avail < uint32_t(kTakeMin)) n = 0;
+          done = (fd >= fd_target && avail == 0) ? 1 : 0;
+          if (pc.contributors > 1) {
+            const unsigned long long gt =
+                *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[pc.r]);
+            if (gt > theta) atomicMax(&st.theta[par], gt);
+          }
+          if (n > 0 || done) break;
+          if (++it > kWaitLimit) {
+            timed_out = true;
+            done = 1;
+            break;
+          }
+          __nanosleep(256);
         }
+        st.sel_n = n;
+        st.sel_done = done;
       }
       Sel::sync();
       const int n = st.sel_n;
@@ -1071,23 +1134,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (sth > theta) theta = sth;
       Sel::sync();
       if (done) break;
-      if (n > 0) {
-        idle = 0;
-        take(n);
-        if (tray_n >= kTrayMark) process_tray(true, pc);
-        else if (tray_n >= pruned + kPruneStep) process_tray(false, pc);
-      } else {
-        if (++idle > kWaitLimit) {
-          timed_out = true;
-          break;
-        }
-        __nanosleep(64);
-      }
+      take(n);
+      if (tray_n >= kTrayMark) process_tray(true, false, pc);
+      else if (tray_n >= pruned + kPruneStep) process_tray(false, false, pc);
     }
 
     // end of the piece: final sort, then the row's output (directly, or
     // through the split-row ticket)
-    if (tray_n > 0) process_tray(true, pc);
+    if (tray_n > 0) process_tray(true, true, pc);
     if (stt == 0) {
       atomicAdd(&p.sorts[pc.r], nsorts);
       atomicAdd(&p.survivors[pc.r], nsorted);
