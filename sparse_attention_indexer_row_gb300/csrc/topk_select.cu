@@ -24,14 +24,15 @@
 //        order, publishes a descriptor per piece and per stage and issues
 //        the copies;
 //      - filter warps test every element against the piece's threshold and
-//        append survivors to the piece's inbox.  On the first stage of each
-//        piece they also set the piece's starting threshold (warm start):
-//        every filter warp finds, by bisection over key bits, a key that at
-//        least ceil(k/8) of its 1024 elements reach, and the smallest of the
-//        eight keys is reached by at least k elements of the piece;
-//      - selector warps drain the inbox into the tray, raise the threshold
-//        (histogram select + prune), run the bitonic tray sort when the tray
-//        passes its mark, and finish each piece.
+//        append survivors to the piece's inbox;
+//      - selector warps set each piece's starting threshold as soon as its
+//        first unit has landed (warm start: every selector warp finds, by
+//        bisection over key bits, a key that at least ceil(k/8) of its 1024
+//        elements of that unit reach, and the smallest of the eight keys is
+//        reached by at least k elements of the piece), drain the inbox into
+//        the tray, raise the threshold (histogram select + prune), run the
+//        bitonic tray sort when the tray passes its mark, and finish each
+//        piece.
 //    Pieces alternate between two inboxes, so the selectors finish piece j
 //    (final sort, output or split-row merge) while the filters already
 //    stream piece j+1; the filters wait only before piece j+2.
@@ -259,6 +260,7 @@ struct Piece {
   int32_t slot;          // partial slot when split
   int32_t first_cta;     // kPlanFlat: first CTA of the row
   int32_t self;          // this CTA's contributor index within the row
+  uint32_t g_first;      // ring stage count at the piece's first stage
 };
 
 struct SmemLayout {
@@ -305,8 +307,9 @@ struct CtaState {
   int leader;                // this CTA drew the last ticket
   int sel_b, sel_above, sel_binc;  // histogram select: chosen bin and counts
   int sel_n, sel_done;             // selector step: words to take, piece done
-  uint32_t est[2][kNF];            // warm start: per filter warp key bound
-  int est_cnt[2];                  // warm start: bounds posted for pieces of parity p
+  uint32_t est[kNS];               // warm start: per selector warp key bound
+  int warm_pub;                    // pieces whose starting threshold is set
+  int first_issued;                // pieces whose first stage the producer has issued
   unsigned long long theta[2];     // threshold word of the piece using inbox p
   Piece table[kTable];             // piece descriptors, by sequence number
 };
@@ -422,6 +425,76 @@ __device__ void build_visit_order_warp(uint32_t* perm, int m, int64_t first, int
   __syncwarp();
 }
 
+// Bitonic network, largest first, over the n = T::size * E words a[0, n),
+// held in registers while it runs: thread t keeps words tE .. tE+E-1.
+// Strides below E compare registers of one thread, strides below 32E
+// exchange through warp shuffles, longer strides (between warps) go through
+// the array with two team barriers each.  Merge levels below first_size are
+// skipped: first_size = 2 sorts, first_size = n merges one bitonic
+// sequence.  The caller has made a[] visible to the team; the result is
+// stored back and followed by a team barrier.
+template <class T, int E>
+__device__ void team_bitonic(uint64_t* a, int first_size, int t) {
+  constexpr int n = T::size * E;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = a[t * E + e];
+#pragma unroll
+  for (int size = 2; size <= n; size <<= 1) {
+    if (size < first_size) continue;
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride < E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & stride) == 0) {
+            const bool larger_first = ((t * E + e) & size) == 0;
+            const uint64_t x = v[e], y = v[e | stride];
+            const bool sw = larger_first ? (x < y) : (x > y);
+            v[e] = sw ? y : x;
+            v[e | stride] = sw ? x : y;
+          }
+        }
+      } else if (stride < 32 * E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = t * E + e;
+          const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v[e], stride / E);
+          const bool keep_max = ((i & stride) == 0) == ((i & size) == 0);
+          v[e] = keep_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[t * E + e] = v[e];
+        T::sync();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = t * E + e;
+          const uint64_t o = a[i ^ stride];
+          const bool keep_max = ((i & stride) == 0) == ((i & size) == 0);
+          v[e] = keep_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+        }
+        T::sync();
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) a[t * E + e] = v[e];
+  T::sync();
+}
+
+// Largest-first bitonic network over n (a power of two) words of a[]:
+// first_size = 2 sorts, first_size = n merges a bitonic sequence.  Ends with
+// a team barrier.
+template <class T>
+__device__ void team_sort_desc(uint64_t* a, int n, int first_size, int t) {
+  static_assert(T::size == 256, "register networks are laid out for 256 threads");
+  if (n == 256) team_bitonic<T, 1>(a, first_size, t);
+  else if (n == 512) team_bitonic<T, 2>(a, first_size, t);
+  else if (n == 1024) team_bitonic<T, 4>(a, first_size, t);
+  else bitonic_network<T, uint64_t, true>(a, n, first_size, 1, 0, t);
+}
+
 // Merge a sorted-descending `batch` of n words (read as if padded with empty
 // words to kp) into the kept list: the best kp of both end up sorted in kept.
 template <class T>
@@ -432,7 +505,7 @@ __device__ void merge_into_kept(uint64_t* kept, const uint64_t* batch, int n, in
     kept[j] = a > b ? a : b;
   }
   T::sync();
-  bitonic_network<T, uint64_t, true>(kept, kp, kp, 1, 0, t);
+  team_sort_desc<T>(kept, kp, kp, t);
 }
 
 __device__ __forceinline__ void write_row(const Params& p, int32_t r, const uint64_t* kept, int t,
@@ -451,10 +524,49 @@ __device__ __forceinline__ void write_row(const Params& p, int32_t r, const uint
   }
 }
 
-// Warm start, per filter warp: the largest key T (its low 16 bits zero) that
-// at least m of the warp's valid, non-NaN elements reach, or 0 when the warp
-// holds fewer than m of them.  Bisection over the key bits from the top, one
-// warp-wide count per bit.
+// One thread's share of a stage: elements 4 * (t + 256 u) + c, u < 8, c < 4.
+// A full, aligned unit is read from shared memory only; otherwise elements
+// past the copied prefix come from global memory and elements past the
+// unit's end are marked invalid (bit e of the result clear).
+__device__ __forceinline__ uint32_t load_share(float (&x)[kEPT], const float* src, const float* row,
+                                               uint32_t e0, uint32_t nvalid, uint32_t copied,
+                                               int t) {
+  if (copied == uint32_t(kUnit)) {
+#pragma unroll
+    for (int u = 0; u < kF4; ++u) {
+      const float4 v = reinterpret_cast<const float4*>(src)[t + kNFT * u];
+      x[4 * u + 0] = v.x;
+      x[4 * u + 1] = v.y;
+      x[4 * u + 2] = v.z;
+      x[4 * u + 3] = v.w;
+    }
+    return 0xFFFFFFFFu;
+  }
+  uint32_t valid = 0u;
+#pragma unroll
+  for (int u = 0; u < kF4; ++u) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t pos = uint32_t(4 * (t + kNFT * u) + c);
+      float v = 0.f;
+      if (pos < copied) v = src[pos];
+      else if (pos < nvalid) v = __ldg(row + e0 + pos);
+      x[4 * u + c] = v;
+      valid |= uint32_t(pos < nvalid) << (4 * u + c);
+    }
+  }
+  return valid;
+}
+
+// Warm start, per warp: a key T (its low 16 bits zero) that at least m of
+// the warp's valid, non-NaN elements reach -- as large as the search below
+// finds -- or 0 when there is none.  A 4-ary search over key bits 31..16:
+// each step tries three keys and counts, warp-wide, the elements at or
+// above each (the three counts packed into one reduction).  For m <= 64
+// the counts run over the union of every lane's four largest keys (128
+// values): T is then reached by at least m real elements, and it falls
+// short of the exact bound only when some lane holds more than four of the
+// warp's top m.
 __device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint32_t valid, int m) {
   uint32_t key[kEPT];
   uint32_t ok = 0;
@@ -466,19 +578,51 @@ __device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint3
     ok += use ? 1u : 0u;
   }
   if (__reduce_add_sync(0xFFFFFFFFu, ok) < uint32_t(m)) return 0u;
+  const uint32_t mm = uint32_t(m);
   uint32_t T = 0;
-#pragma unroll 1
-  for (int b = 31; b >= 16; --b) {
-    const uint32_t t = T | (1u << b);
-    uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+  if (m <= 64) {
+    uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;  // this lane's four largest, l0 >= .. >= l3
 #pragma unroll
-    for (int e = 0; e < kEPT; e += 4) {
-      c0 += key[e + 0] >= t ? 1u : 0u;
-      c1 += key[e + 1] >= t ? 1u : 0u;
-      c2 += key[e + 2] >= t ? 1u : 0u;
-      c3 += key[e + 3] >= t ? 1u : 0u;
+    for (int e = 0; e < kEPT; ++e) {
+      const uint32_t v = key[e];
+      const uint32_t a3 = max(l3, min(l2, v));
+      const uint32_t a2 = max(l2, min(l1, v));
+      const uint32_t a1 = max(l1, min(l0, v));
+      l0 = max(l0, v);
+      l1 = a1;
+      l2 = a2;
+      l3 = a3;
     }
-    if (__reduce_add_sync(0xFFFFFFFFu, (c0 + c1) + (c2 + c3)) >= uint32_t(m)) T = t;
+#pragma unroll 1
+    for (int b = 31; b >= 17; b -= 2) {
+      uint32_t pk = 0;  // three counts of at most 128, eight bits each
+#pragma unroll
+      for (uint32_t i = 1; i <= 3; ++i) {
+        const uint32_t t = T | (i << (b - 1));
+        pk += ((l0 >= t ? 1u : 0u) + (l1 >= t ? 1u : 0u) + (l2 >= t ? 1u : 0u) +
+               (l3 >= t ? 1u : 0u)) << (8 * (i - 1));
+      }
+      pk = __reduce_add_sync(0xFFFFFFFFu, pk);
+      const uint32_t i = ((pk >> 16) & 0xFFu) >= mm ? 3u
+                         : ((pk >> 8) & 0xFFu) >= mm ? 2u
+                         : (pk & 0xFFu) >= mm ? 1u : 0u;
+      T |= i << (b - 1);
+    }
+    return T;
+  }
+#pragma unroll 1
+  for (int b = 31; b >= 17; b -= 2) {
+    const uint32_t t1 = T | (1u << (b - 1)), t2 = T | (2u << (b - 1)), t3 = T | (3u << (b - 1));
+    uint32_t c12 = 0, c3 = 0;  // counts of at most 1024: two per word, sixteen bits each
+#pragma unroll
+    for (int e = 0; e < kEPT; ++e) {
+      c12 += (key[e] >= t1 ? 1u : 0u) + (key[e] >= t2 ? 0x10000u : 0u);
+      c3 += key[e] >= t3 ? 1u : 0u;
+    }
+    c12 = __reduce_add_sync(0xFFFFFFFFu, c12);
+    c3 = __reduce_add_sync(0xFFFFFFFFu, c3);
+    const uint32_t i = c3 >= mm ? 3u : (c12 >> 16) >= mm ? 2u : (c12 & 0xFFFFu) >= mm ? 1u : 0u;
+    T |= i << (b - 1);
   }
   return T;
 }
@@ -518,12 +662,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       st.head[q] = 0;
       st.tail[q] = 0;
       st.fdone[q] = 0;
-      st.est_cnt[q] = 0;
       st.theta[q] = 0ull;
     }
     st.sel_pieces = 0;
     st.pieces_pub = 0;
     st.npieces = -1;
+    st.warm_pub = 0;
+    st.first_issued = 0;
     st.flags = 0;
     for (int i = 0; i < nstage; ++i) {
       mbar_init(&full[i], 1);
@@ -571,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           }
           __nanosleep(256);
         }
+        pc.g_first = g;  // the piece's first stage is the next one issued
         st.table[seq % kTable] = pc;
         __threadfence_block();
         *reinterpret_cast<volatile int*>(&st.pieces_pub) = seq + 1;
@@ -589,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         d.tag = uint32_t(seq) | kFirst | kLast;
         desc[stage] = d;
         mbar_arrive(&full[stage]);
+        *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
         advance();
       }
       const int m_row = int((pc.L + kUnit - 1) / kUnit);
@@ -626,6 +773,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             } else {
               mbar_arrive(&full[stage]);
             }
+            // Until a piece's first stage is issued, its ring slot's barrier
+            // may still be in an earlier phase: the selectors look at it only
+            // after this count says the stage is on its way.
+            if (c0 == 0 && i == 0) *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
             advance();
           }
         }
@@ -653,10 +804,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     return;
   }
 
-  // ---------------- filter warps: a4 + a5 and the warm start ----------------
+  // ---------------- filter warps: a4 + a5 ----------------
   if (warp < kNF) {
     const int ft = tid;  // 0 .. kNFT-1
-    const int m_warm = (k + kNF - 1) / kNF;
     uint64_t th = 0ull;
     float thf = threshold_float(th);
     uint32_t admitted = 0;
@@ -677,80 +827,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         break;
       }
       if (d.tag & kEnd) break;
-      const bool first = (d.tag & kFirst) != 0;
-      int seq = 0;
-      if (first) {
-        seq = int(d.tag & kSeqMask);
+      if (d.tag & kFirst) {
+        const int seq = int(d.tag & kSeqMask);
         par = seq & 1;
-        // this parity's inbox, counters and threshold are free again once the
-        // selectors have finished piece seq - 2
-        if (seq >= 2) {
-          if (lane == 0) {
-            uint32_t it = 0;
-            while (*reinterpret_cast<volatile int*>(&st.sel_pieces) < seq - 1) {
-              if (++it > kWaitLimit) {
-                timed_out = true;
-                break;
-              }
-              __nanosleep(128);
-            }
-          }
-          if (__any_sync(0xFFFFFFFFu, timed_out)) {
-            timed_out = true;
-            break;
-          }
-        }
-        r = int32_t(d.r);
-        row = p.scores + int64_t(r) * p.row_stride;
-        aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-      } else {
-        const uint64_t nt = *reinterpret_cast<volatile unsigned long long*>(&st.theta[par]);
-        if (nt != th) {
-          th = nt;
-          thf = threshold_float(th);
-        }
-      }
-      const float* src = ring + stage * kUnit;
-      const uint32_t e0 = d.e0, nvalid = d.nvalid;
-      const uint32_t copied = aligned ? (nvalid & ~3u) : 0u;
-      float x[kEPT];
-      uint32_t valid = 0xFFFFFFFFu;  // bit e: element e is inside the row
-      if (copied == uint32_t(kUnit)) {
-#pragma unroll
-        for (int u = 0; u < kF4; ++u) {
-          const float4 v = reinterpret_cast<const float4*>(src)[ft + kNFT * u];
-          x[4 * u + 0] = v.x;
-          x[4 * u + 1] = v.y;
-          x[4 * u + 2] = v.z;
-          x[4 * u + 3] = v.w;
-        }
-      } else {
-        valid = 0u;
-#pragma unroll
-        for (int u = 0; u < kF4; ++u) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t pos = uint32_t(4 * (ft + kNFT * u) + c);
-            float v = 0.f;
-            if (pos < copied) v = src[pos];
-            else if (pos < nvalid) v = __ldg(row + e0 + pos);
-            x[4 * u + c] = v;
-            valid |= uint32_t(pos < nvalid) << (4 * u + c);
-          }
-        }
-      }
-      if (first) {
-        // warm start: each warp bounds its share, the smallest bound holds
-        // for the piece (k elements reach it)
-        const uint32_t est = warp_key_bound(x, valid, m_warm);
+        // The selectors set the piece's starting threshold once this unit
+        // has landed, and only after piece seq - 2 (which used the same
+        // inbox, counters and threshold word) is finished.
         if (lane == 0) {
-          *reinterpret_cast<volatile uint32_t*>(&st.est[par][warp]) = est;
-          __threadfence_block();
-          atomicAdd(&st.est_cnt[par], 1);
-          // every filter warp posts a bound for every piece; wait for the other seven
-          const int target = kNF * (seq / 2 + 1);
           uint32_t it = 0;
-          while (*reinterpret_cast<volatile int*>(&st.est_cnt[par]) < target) {
+          while (*reinterpret_cast<volatile int*>(&st.warm_pub) < seq + 1) {
             if (++it > kWaitLimit) {
               timed_out = true;
               break;
@@ -762,22 +847,23 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           timed_out = true;
           break;
         }
-        __threadfence_block();  // the other warps' bounds are read after their count
-        uint32_t mk = 0xFFFFFFFFu;
-#pragma unroll
-        for (int w = 0; w < kNF; ++w)
-          mk = min(mk, *reinterpret_cast<volatile uint32_t*>(&st.est[par][w]));
-        th = mk ? (uint64_t(mk) << 32) - 1ull : 0ull;
-        if (warp == 0 && lane == 0 && th) {
-          unsigned long long t = th;
-          if (st.table[seq % kTable].contributors > 1) {
-            const unsigned long long old = atomicMax(&p.row_theta[r], t);
-            if (old > t) t = old;
-          }
-          atomicMax(&st.theta[par], t);
-        }
+        r = int32_t(d.r);
+        row = p.scores + int64_t(r) * p.row_stride;
+        aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+        th = *reinterpret_cast<volatile unsigned long long*>(&st.theta[par]);
         thf = threshold_float(th);
+      } else {
+        const uint64_t nt = *reinterpret_cast<volatile unsigned long long*>(&st.theta[par]);
+        if (nt != th) {
+          th = nt;
+          thf = threshold_float(th);
+        }
       }
+      const float* src = ring + stage * kUnit;
+      const uint32_t e0 = d.e0, nvalid = d.nvalid;
+      const uint32_t copied = aligned ? (nvalid & ~3u) : 0u;
+      float x[kEPT];
+      const uint32_t valid = load_share(x, src, row, e0, nvalid, copied, ft);  // bit e: in the row
       // Most stages have no element past the threshold: one chained float
       // test first (a superset: it also passes NaN, ties and padding), the
       // per-element mask only when some lane needs it.
@@ -791,21 +877,28 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         m3 |= !(x[4 * u + 3] < thf);
       }
       if (__any_sync(0xFFFFFFFFu, (m0 | m1) | (m2 | m3))) {
-        uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;  // bit e: element e may beat the threshold
+        // A strict float compare is already the exact word test for every
+        // value except NaN and values equal to the threshold's own (ties,
+        // and -0.0 against +0.0): those few get the 64-bit word test.
+        uint32_t g0 = 0, g1 = 0, g2 = 0, g3 = 0;  // bit e: x[e] > the threshold value
+        uint32_t q0 = 0, q1 = 0, q2 = 0, q3 = 0;  // bit e: x[e] equal to it, or NaN
 #pragma unroll
         for (int u = 0; u < kF4; ++u) {
-          c0 |= uint32_t(!(x[4 * u + 0] < thf)) << (4 * u + 0);
-          c1 |= uint32_t(!(x[4 * u + 1] < thf)) << (4 * u + 1);
-          c2 |= uint32_t(!(x[4 * u + 2] < thf)) << (4 * u + 2);
-          c3 |= uint32_t(!(x[4 * u + 3] < thf)) << (4 * u + 3);
+          g0 |= uint32_t(x[4 * u + 0] > thf) << (4 * u + 0);
+          g1 |= uint32_t(x[4 * u + 1] > thf) << (4 * u + 1);
+          g2 |= uint32_t(x[4 * u + 2] > thf) << (4 * u + 2);
+          g3 |= uint32_t(x[4 * u + 3] > thf) << (4 * u + 3);
+          q0 |= uint32_t(!(x[4 * u + 0] < thf) && !(x[4 * u + 0] > thf)) << (4 * u + 0);
+          q1 |= uint32_t(!(x[4 * u + 1] < thf) && !(x[4 * u + 1] > thf)) << (4 * u + 1);
+          q2 |= uint32_t(!(x[4 * u + 2] < thf) && !(x[4 * u + 2] > thf)) << (4 * u + 2);
+          q3 |= uint32_t(!(x[4 * u + 3] < thf) && !(x[4 * u + 3] > thf)) << (4 * u + 3);
         }
-        const uint32_t cand = ((c0 | c1) | (c2 | c3)) & valid;
-        // Exact word test of the flagged elements.  On a full stage each lane
-        // walks only its own set bits, re-reading them from the stage (not
-        // released yet); a ragged stage has its values in registers already
-        // and takes a fixed walk over all of them.  Then each lane with
-        // survivors reserves its own run of inbox slots (one shared-memory
-        // atomicAdd) and writes them.
+        uint32_t passm = ((g0 | g1) | (g2 | g3)) & valid;
+        const uint32_t rare = ((q0 | q1) | (q2 | q3)) & valid;
+        // On a full stage the values are re-read from the stage (not released
+        // yet); a ragged stage has them in registers and takes a fixed walk.
+        // Then each lane with survivors reserves its own run of inbox slots
+        // (one shared-memory atomicAdd) and writes them.
         const bool clean = copied == uint32_t(kUnit);
         auto word_of = [&](uint32_t bits, int e) -> uint64_t {
           const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
@@ -814,23 +907,24 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         auto smem_bits = [&](int e) -> uint32_t {
           return __float_as_uint(src[4 * (ft + kNFT * (e >> 2)) + (e & 3)]);
         };
-        uint32_t passm = 0;
-        if (clean) {
-          for (uint32_t mm = cand; mm; mm &= mm - 1u) {
-            const int e = __ffs(mm) - 1;
-            const uint32_t bits = smem_bits(e);
-            const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
-            saw_nan |= nan;
-            if (!nan && word_of(bits, e) > th) passm |= 1u << e;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < kEPT; ++e) {
-            if ((cand >> e) & 1u) {
-              const uint32_t bits = __float_as_uint(x[e]);
+        if (rare) {
+          if (clean) {
+            for (uint32_t mm = rare; mm; mm &= mm - 1u) {
+              const int e = __ffs(mm) - 1;
+              const uint32_t bits = smem_bits(e);
               const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
               saw_nan |= nan;
               if (!nan && word_of(bits, e) > th) passm |= 1u << e;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < kEPT; ++e) {
+              if ((rare >> e) & 1u) {
+                const uint32_t bits = __float_as_uint(x[e]);
+                const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+                saw_nan |= nan;
+                if (!nan && word_of(bits, e) > th) passm |= 1u << e;
+              }
             }
           }
         }
@@ -904,6 +998,46 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   uint64_t theta = 0ull;
   uint32_t head[2] = {0u, 0u};
   int par = 0;
+  int warm_next = 0;  // next piece whose starting threshold is to be set
+  const int m_warm = (k + kNS - 1) / kNS;
+
+  // Warm start of piece w, whose first unit has landed in the ring (the
+  // filters hold it until the threshold is set): each selector warp bounds
+  // its 1024 elements of the unit, the smallest bound is reached by at least
+  // k elements of the piece.  The piece may use the threshold word of its
+  // parity: the piece before it in that parity is finished.
+  auto warm_start = [&](int w) {
+    const Piece pw = st.table[w % kTable];
+    const int slot = int(pw.g_first % uint32_t(nstage));
+    // every reader observes the copy's completion itself (already complete)
+    if (!mbar_wait(&full[slot], (pw.g_first / uint32_t(nstage)) & 1u, kWaitLimit)) timed_out = true;
+    const StageDesc d = desc[slot];
+    const float* wrow = p.scores + int64_t(pw.r) * p.row_stride;
+    const bool waligned = (reinterpret_cast<uintptr_t>(wrow) & 15u) == 0;
+    float x[kEPT];
+    const uint32_t valid = load_share(x, ring + slot * kUnit, wrow, d.e0, d.nvalid,
+                                      waligned ? (d.nvalid & ~3u) : 0u, stt);
+    const uint32_t est = warp_key_bound(x, valid, m_warm);
+    if (lane == 0) st.est[swarp] = est;
+    Sel::sync();
+    uint32_t mk = 0xFFFFFFFFu;
+#pragma unroll
+    for (int q = 0; q < kNS; ++q) mk = min(mk, st.est[q]);
+    if (stt == 0) {
+      const uint64_t th0 = mk ? (uint64_t(mk) << 32) - 1ull : 0ull;
+      if (th0) {
+        unsigned long long t = th0;
+        if (pw.contributors > 1) {
+          const unsigned long long old = atomicMax(&p.row_theta[pw.r], t);
+          if (old > t) t = old;
+        }
+        atomicMax(&st.theta[w & 1], t);
+      }
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&st.warm_pub) = w + 1;
+    }
+    Sel::sync();  // the bounds are read before the next warm start rewrites them
+  };
 
   // Publish a threshold to the filters (and to the row's other CTAs).
   auto raise_theta = [&](uint64_t nth, const Piece& pc) {
@@ -1019,11 +1153,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       raise_theta(T ? T - 1ull : 0ull, pc);
       return;
     }
-    // the bitonic tray sort: sort the r survivors and merge them in
-    const int P = next_pow2_dev(max(r, 1));
+    // the bitonic tray sort: sort the r survivors (padded with empty words
+    // to a power of two, at least one word per selector thread) and merge
+    // them in
+    const int P = max(next_pow2_dev(max(r, 1)), kNST);
     for (int t = r + stt; t < P; t += kNST) tray[t] = 0ull;
     Sel::sync();
-    bitonic_network<Sel, uint64_t, true>(tray, P, 2, 1, 0, stt);
+    team_sort_desc<Sel>(tray, P, 2, stt);
     if (kept_n == 0) {
       // nothing kept yet: the sorted tray is the list
       for (int q = stt; q < kp; q += kNST) kept[q] = q < P ? tray[q] : 0ull;
@@ -1102,8 +1238,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       // is read before the tail, so a full count means the tail is final.
       if (stt == 0) {
         uint32_t it = timed_out ? kWaitLimit : 0u;
-        int n = 0, done = 0;
+        int n = 0, done = 0, warm = 0;
         for (;;) {
+          // first: a piece (this one or the next) whose first unit has
+          // landed and still waits for its starting threshold
+          if (warm_next <= j + 1 &&
+              *reinterpret_cast<volatile int*>(&st.first_issued) > warm_next) {
+            const uint32_t gf = st.table[warm_next % kTable].g_first;
+            if (mbar_try_wait(&full[gf % uint32_t(nstage)], (gf / uint32_t(nstage)) & 1u)) {
+              warm = 1;
+              break;
+            }
+          }
           const int fd = *reinterpret_cast<volatile int*>(&st.fdone[par]);
           const uint32_t tail = *reinterpret_cast<volatile uint32_t*>(&st.tail[par]);
           const uint32_t avail = tail - head[par];
@@ -1126,13 +1272,20 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         }
         st.sel_n = n;
         st.sel_done = done;
+        st.flags = warm;
       }
       Sel::sync();
       const int n = st.sel_n;
       const bool done = st.sel_done != 0;
+      const bool warm = st.flags != 0;
       const uint64_t sth = *reinterpret_cast<volatile unsigned long long*>(&st.theta[par]);
       if (sth > theta) theta = sth;
       Sel::sync();
+      if (warm) {
+        warm_start(warm_next);
+        ++warm_next;
+        continue;
+      }
       if (done) break;
       take(n);
       if (tray_n >= kTrayMark) process_tray(true, false, pc);
@@ -1202,7 +1355,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               a[q] = x > y ? x : y;
             }
             Sel::sync();
-            bitonic_network<Sel, uint64_t, true>(slots, kp, kp, npairs, 2 * gap * kp, stt);
+            if (kp >= kNST) {
+              for (int pr = 0; pr < npairs; ++pr)
+                team_sort_desc<Sel>(slots + (2 * gap * pr) * kp, kp, kp, stt);
+            } else {
+              bitonic_network<Sel, uint64_t, true>(slots, kp, kp, npairs, 2 * gap * kp, stt);
+            }
           }
         }
         write_row(p, pc.r, slots, stt, kNST);
