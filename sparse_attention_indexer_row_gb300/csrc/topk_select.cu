@@ -94,6 +94,10 @@ constexpr int kPermChunk = 256;              // units shuffled together (2M elem
 constexpr int kTrayMark = 2048;              // tray words that trigger the tray sort
 constexpr int kPruneStep = 512;              // new tray words that trigger a prune
 constexpr int kSelectSlack = 256;            // extra words a pruned tray may keep
+constexpr int kWarmUnits = 4;                // units a warm start reads (k <= 512)
+// (k <= 512 runs a five-stage ring: the producer can land all warm-start
+// units of a piece while the filters hold its first one)
+static_assert(kWarmUnits <= 5, "warm-start units fit in the ring");
 constexpr int kMaxSplit = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls before a wait gives up
 
@@ -558,33 +562,32 @@ __device__ __forceinline__ uint32_t load_share(float (&x)[kEPT], const float* sr
   return valid;
 }
 
-// Warm start, per warp: a key T (its low 16 bits zero) that at least m of
-// the warp's valid, non-NaN elements reach -- as large as the search below
-// finds -- or 0 when there is none.  A 4-ary search over key bits 31..16:
-// each step tries three keys and counts, warp-wide, the elements at or
-// above each (the three counts packed into one reduction).  For m <= 64
-// the counts run over the union of every lane's four largest keys (128
-// values): T is then reached by at least m real elements, and it falls
-// short of the exact bound only when some lane holds more than four of the
-// warp's top m.
-__device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint32_t valid, int m) {
-  uint32_t key[kEPT];
-  uint32_t ok = 0;
-#pragma unroll
-  for (int e = 0; e < kEPT; ++e) {
-    const uint32_t bits = __float_as_uint(x[e]);
-    const bool use = ((valid >> e) & 1u) && (bits & 0x7FFFFFFFu) <= 0x7F800000u;
-    key[e] = use ? order_key(bits) : 0u;
-    ok += use ? 1u : 0u;
-  }
-  if (__reduce_add_sync(0xFFFFFFFFu, ok) < uint32_t(m)) return 0u;
-  const uint32_t mm = uint32_t(m);
-  uint32_t T = 0;
-  if (m <= 64) {
-    uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;  // this lane's four largest, l0 >= .. >= l3
+// Warm start.  A key T (its low 16 bits zero) that at least m valid,
+// non-NaN elements reach is a valid starting threshold word (T << 32) - 1
+// for a piece once m * 8 = k of the piece's elements are known to reach the
+// smallest of the eight warps' keys.  Each warp searches a 4-ary way over key
+// bits 31..16: a step tries three keys and counts, warp-wide, the elements
+// at or above each (the three counts packed into one reduction).
+
+// Key of element e of a thread's share, or 0 for padding and NaN.
+__device__ __forceinline__ uint32_t share_key(const float (&x)[kEPT], uint32_t valid, int e) {
+  const uint32_t bits = __float_as_uint(x[e]);
+  const bool use = ((valid >> e) & 1u) && (bits & 0x7FFFFFFFu) <= 0x7F800000u;
+  return use ? order_key(bits) : 0u;
+}
+
+// For m <= 64 the counts run over the union of every lane's four largest
+// keys (128 values per warp): T is reached by at least m real elements, and
+// falls short of the exact bound only when some lane holds more than four
+// of the warp's top m.  Lane lists are kept sorted, l0 >= l1 >= l2 >= l3.
+struct Top4 {
+  uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;
+  uint32_t real = 0;  // valid, non-NaN elements seen by this lane
+  __device__ __forceinline__ void add(const float (&x)[kEPT], uint32_t valid) {
 #pragma unroll
     for (int e = 0; e < kEPT; ++e) {
-      const uint32_t v = key[e];
+      const uint32_t v = share_key(x, valid, e);
+      real += v != 0u ? 1u : 0u;
       const uint32_t a3 = max(l3, min(l2, v));
       const uint32_t a2 = max(l2, min(l1, v));
       const uint32_t a1 = max(l1, min(l0, v));
@@ -593,6 +596,11 @@ __device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint3
       l2 = a2;
       l3 = a3;
     }
+  }
+  __device__ __forceinline__ uint32_t bound(int m) const {
+    if (__reduce_add_sync(0xFFFFFFFFu, real) < uint32_t(m)) return 0u;
+    const uint32_t mm = uint32_t(m);
+    uint32_t T = 0;
 #pragma unroll 1
     for (int b = 31; b >= 17; b -= 2) {
       uint32_t pk = 0;  // three counts of at most 128, eight bits each
@@ -610,6 +618,20 @@ __device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint3
     }
     return T;
   }
+};
+
+// For m > 64 the counts run over all 32 keys of each lane (one unit).
+__device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint32_t valid, int m) {
+  uint32_t key[kEPT];
+  uint32_t ok = 0;
+#pragma unroll
+  for (int e = 0; e < kEPT; ++e) {
+    key[e] = share_key(x, valid, e);
+    ok += key[e] != 0u ? 1u : 0u;
+  }
+  if (__reduce_add_sync(0xFFFFFFFFu, ok) < uint32_t(m)) return 0u;
+  const uint32_t mm = uint32_t(m);
+  uint32_t T = 0;
 #pragma unroll 1
   for (int b = 31; b >= 17; b -= 2) {
     const uint32_t t1 = T | (1u << (b - 1)), t2 = T | (2u << (b - 1)), t3 = T | (3u << (b - 1));
@@ -625,6 +647,14 @@ __device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint3
     T |= i << (b - 1);
   }
   return T;
+}
+
+// Units a piece's warm start reads: kWarmUnits (at most the piece's units)
+// when each warp needs at most 64 elements (k <= 512), else one.
+__host__ __device__ inline int warm_units(int k, int nu) {
+  const int m = (k + kNS - 1) / kNS;
+  if (m > 64) return 1;
+  return nu < 1 ? 1 : (nu < kWarmUnits ? nu : kWarmUnits);
 }
 
 // ---------------------------------------------------------------------------
@@ -740,18 +770,23 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       }
       const int m_row = int((pc.L + kUnit - 1) / kUnit);
       const bool partial_tail = (pc.L % uint32_t(kUnit)) != 0;
+      const int wu = warm_units(p.k, nu);
       for (int c0 = 0; c0 < nu; c0 += kPermChunk) {
         const int cs = min(nu - c0, kPermChunk);
         build_visit_order_warp(perm, cs, int64_t(pc.u_begin) + c0, pc.r, p.seed_lo, p.seed_hi,
                                identity, lane);
         if (lane == 0) {
-          // Visit a full unit first (the warm start reads the first unit): if
-          // the order opens with the row's short last unit, swap the first two.
-          if (c0 == 0 && cs > 1 && partial_tail &&
-              pc.u_begin + int(perm[0] & uint32_t(kPermChunk - 1)) == m_row - 1) {
-            const uint32_t t0 = perm[0];
-            perm[0] = perm[1];
-            perm[1] = t0;
+          // Full units first (the warm start reads the first wu units): if
+          // the row's short last unit is among them and the piece has more,
+          // swap it with the unit after them.
+          if (c0 == 0 && cs > wu && partial_tail) {
+            for (int q = 0; q < wu; ++q) {
+              if (pc.u_begin + int(perm[q] & uint32_t(kPermChunk - 1)) == m_row - 1) {
+                const uint32_t t0 = perm[q];
+                perm[q] = perm[wu];
+                perm[wu] = t0;
+              }
+            }
           }
           for (int i = 0; i < cs; ++i) {
             next_slot();
@@ -773,10 +808,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             } else {
               mbar_arrive(&full[stage]);
             }
-            // Until a piece's first stage is issued, its ring slot's barrier
-            // may still be in an earlier phase: the selectors look at it only
-            // after this count says the stage is on its way.
-            if (c0 == 0 && i == 0) *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
+            // Until a piece's first wu stages are issued, their ring slots'
+            // barriers may still be in an earlier phase: the selectors look at
+            // them only after this count says the stages are on their way.
+            if (c0 + i == wu - 1) *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
             advance();
           }
         }
@@ -1001,23 +1036,31 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   int warm_next = 0;  // next piece whose starting threshold is to be set
   const int m_warm = (k + kNS - 1) / kNS;
 
-  // Warm start of piece w, whose first unit has landed in the ring (the
-  // filters hold it until the threshold is set): each selector warp bounds
-  // its 1024 elements of the unit, the smallest bound is reached by at least
-  // k elements of the piece.  The piece may use the threshold word of its
+  // Warm start of piece w, whose first units have landed in the ring (the
+  // filters hold them until the threshold is set): each selector warp bounds
+  // its share of those units, the smallest bound is reached by at least k
+  // elements of the piece.  The piece may use the threshold word of its
   // parity: the piece before it in that parity is finished.
   auto warm_start = [&](int w) {
     const Piece pw = st.table[w % kTable];
-    const int slot = int(pw.g_first % uint32_t(nstage));
-    // every reader observes the copy's completion itself (already complete)
-    if (!mbar_wait(&full[slot], (pw.g_first / uint32_t(nstage)) & 1u, kWaitLimit)) timed_out = true;
-    const StageDesc d = desc[slot];
+    const int wu = warm_units(k, pw.u_end - pw.u_begin);
     const float* wrow = p.scores + int64_t(pw.r) * p.row_stride;
     const bool waligned = (reinterpret_cast<uintptr_t>(wrow) & 15u) == 0;
-    float x[kEPT];
-    const uint32_t valid = load_share(x, ring + slot * kUnit, wrow, d.e0, d.nvalid,
-                                      waligned ? (d.nvalid & ~3u) : 0u, stt);
-    const uint32_t est = warp_key_bound(x, valid, m_warm);
+    uint32_t est = 0;
+    Top4 top;
+    for (int q = 0; q < wu; ++q) {
+      const uint32_t g = pw.g_first + uint32_t(q);
+      const int slot = int(g % uint32_t(nstage));
+      // every reader observes the copy's completion itself (already complete)
+      if (!mbar_wait(&full[slot], (g / uint32_t(nstage)) & 1u, kWaitLimit)) timed_out = true;
+      const StageDesc d = desc[slot];
+      float x[kEPT];
+      const uint32_t valid = load_share(x, ring + slot * kUnit, wrow, d.e0, d.nvalid,
+                                        waligned ? (d.nvalid & ~3u) : 0u, stt);
+      if (m_warm <= 64) top.add(x, valid);
+      else est = warp_key_bound(x, valid, m_warm);
+    }
+    if (m_warm <= 64) est = top.bound(m_warm);
     if (lane == 0) st.est[swarp] = est;
     Sel::sync();
     uint32_t mk = 0xFFFFFFFFu;
@@ -1113,7 +1156,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         prefix |= uint64_t(b) << shift;
         greater += above;
         need -= above;
-        if (greater + binc <= uint32_t(kp + slack) || pass == 7) {
+        // a prune stops at a 16-bit key prefix: a bound, not the exact word
+        if (greater + binc <= uint32_t(kp + slack) || pass == 7 || (!sort && pass == 1)) {
           T = prefix;
           break;
         }
@@ -1240,14 +1284,33 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         uint32_t it = timed_out ? kWaitLimit : 0u;
         int n = 0, done = 0, warm = 0;
         for (;;) {
-          // first: a piece (this one or the next) whose first unit has
-          // landed and still waits for its starting threshold
-          if (warm_next <= j + 1 &&
-              *reinterpret_cast<volatile int*>(&st.first_issued) > warm_next) {
-            const uint32_t gf = st.table[warm_next % kTable].g_first;
-            if (mbar_try_wait(&full[gf % uint32_t(nstage)], (gf / uint32_t(nstage)) & 1u)) {
-              warm = 1;
+          // First: a piece (this one or the next) still waiting for its
+          // starting threshold.  A split row whose other CTAs have already
+          // published a threshold starts from that one at once (action 2);
+          // otherwise the warm start runs once its units have landed
+          // (action 1).
+          bool warm_due = false;
+          if (warm_next <= j + 1 && *reinterpret_cast<volatile int*>(&st.pieces_pub) > warm_next) {
+            const Piece& pn = st.table[warm_next % kTable];
+            const unsigned long long rt =
+                pn.contributors > 1
+                    ? *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[pn.r])
+                    : 0ull;
+            if (rt != 0ull) {
+              atomicMax(&st.theta[warm_next & 1], rt);
+              __threadfence_block();
+              *reinterpret_cast<volatile int*>(&st.warm_pub) = warm_next + 1;
+              warm = 2;
               break;
+            }
+            if (*reinterpret_cast<volatile int*>(&st.first_issued) > warm_next) {
+              const uint32_t gl =
+                  pn.g_first + uint32_t(warm_units(k, pn.u_end - pn.u_begin) - 1);
+              if (mbar_try_wait(&full[gl % uint32_t(nstage)], (gl / uint32_t(nstage)) & 1u)) {
+                warm = 1;
+                break;
+              }
+              warm_due = true;  // issued, not landed yet
             }
           }
           const int fd = *reinterpret_cast<volatile int*>(&st.fdone[par]);
@@ -1257,6 +1320,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           if (n > kTakeMax) n = kTakeMax;
           if (fd < fd_target && avail < uint32_t(kTakeMin)) n = 0;
           done = (fd >= fd_target && avail == 0) ? 1 : 0;
+          // the filters wait on the next piece's threshold, not on this
+          // piece's end: a warm start whose units are on their way goes first
+          if (done && warm_due) done = 0;
           if (pc.contributors > 1) {
             const unsigned long long gt =
                 *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[pc.r]);
@@ -1277,12 +1343,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       Sel::sync();
       const int n = st.sel_n;
       const bool done = st.sel_done != 0;
-      const bool warm = st.flags != 0;
+      const int warm = st.flags;
       const uint64_t sth = *reinterpret_cast<volatile unsigned long long*>(&st.theta[par]);
       if (sth > theta) theta = sth;
       Sel::sync();
       if (warm) {
-        warm_start(warm_next);
+        if (warm == 1) warm_start(warm_next);
         ++warm_next;
         continue;
       }
