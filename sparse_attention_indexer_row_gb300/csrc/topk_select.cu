@@ -374,13 +374,15 @@ __device__ int get_piece(const Params& p, int32_t pi, Piece& out, bool& bad_len)
 // starting at unit `first`, drawn by one warp: the units sorted by a Philox
 // draw whose low 8 bits are replaced by the unit's position, so the order is
 // a permutation whatever the draws and never depends on the scores.
-// perm[i] & 255 = position visited i-th.  Key i of the sort sits in lane
-// i % 32, register i / 32; strides of 32 and more swap registers, shorter
-// ones exchange through shuffles.
-__device__ void build_visit_order_warp(uint32_t* perm, int m, int64_t first, int32_t row,
-                                       uint32_t seed_lo, uint32_t seed_hi, bool identity,
-                                       int lane) {
-  constexpr int E = kPermChunk / 32;
+// perm[i] & 255 = position visited i-th.  The sort runs over 32E keys (E
+// the smallest power of two with 32E >= m, empty keys last); key i sits in
+// lane i % 32, register i / 32; strides of 32 and more swap registers,
+// shorter ones exchange through shuffles.
+template <int E>
+__device__ __forceinline__ void visit_order_sort(uint32_t* perm, int m, int64_t first, int32_t row,
+                                                 uint32_t seed_lo, uint32_t seed_hi,
+                                                 bool identity, int lane) {
+  constexpr int n = 32 * E;
   uint32_t v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -398,7 +400,7 @@ __device__ void build_visit_order_warp(uint32_t* perm, int m, int64_t first, int
     v[e] = key;
   }
 #pragma unroll
-  for (int size = 2; size <= kPermChunk; size <<= 1) {
+  for (int size = 2; size <= n; size <<= 1) {
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       if (stride >= 32) {
@@ -427,6 +429,16 @@ __device__ void build_visit_order_warp(uint32_t* perm, int m, int64_t first, int
 #pragma unroll
   for (int e = 0; e < E; ++e) perm[e * 32 + lane] = v[e];
   __syncwarp();
+}
+
+__device__ void build_visit_order_warp(uint32_t* perm, int m, int64_t first, int32_t row,
+                                       uint32_t seed_lo, uint32_t seed_hi, bool identity,
+                                       int lane) {
+  static_assert(kPermChunk == 256, "orders of up to 8 keys per lane");
+  if (m <= 32) visit_order_sort<1>(perm, m, first, row, seed_lo, seed_hi, identity, lane);
+  else if (m <= 64) visit_order_sort<2>(perm, m, first, row, seed_lo, seed_hi, identity, lane);
+  else if (m <= 128) visit_order_sort<4>(perm, m, first, row, seed_lo, seed_hi, identity, lane);
+  else visit_order_sort<8>(perm, m, first, row, seed_lo, seed_hi, identity, lane);
 }
 
 // Bitonic network, largest first, over the n = T::size * E words a[0, n),
@@ -583,19 +595,20 @@ __device__ __forceinline__ uint32_t share_key(const float (&x)[kEPT], uint32_t v
 struct Top4 {
   uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;
   uint32_t real = 0;  // valid, non-NaN elements seen by this lane
-  __device__ __forceinline__ void add(const float (&x)[kEPT], uint32_t valid) {
-#pragma unroll
-    for (int e = 0; e < kEPT; ++e) {
-      const uint32_t v = share_key(x, valid, e);
-      real += v != 0u ? 1u : 0u;
-      const uint32_t a3 = max(l3, min(l2, v));
-      const uint32_t a2 = max(l2, min(l1, v));
-      const uint32_t a1 = max(l1, min(l0, v));
-      l0 = max(l0, v);
-      l1 = a1;
-      l2 = a2;
-      l3 = a3;
-    }
+  // one element (key 0: padding or NaN)
+  __device__ __forceinline__ void add(uint32_t v) {
+    real += v != 0u ? 1u : 0u;
+    const uint32_t a3 = max(l3, min(l2, v));
+    const uint32_t a2 = max(l2, min(l1, v));
+    const uint32_t a1 = max(l1, min(l0, v));
+    l0 = max(l0, v);
+    l1 = a1;
+    l2 = a2;
+    l3 = a3;
+  }
+  __device__ __forceinline__ void add_value(float x) {
+    const uint32_t bits = __float_as_uint(x);
+    add((bits & 0x7FFFFFFFu) <= 0x7F800000u ? order_key(bits) : 0u);
   }
   __device__ __forceinline__ uint32_t bound(int m) const {
     if (__reduce_add_sync(0xFFFFFFFFu, real) < uint32_t(m)) return 0u;
@@ -666,8 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   const SmemLayout sl = smem_layout(p.kp);
   float* ring = reinterpret_cast<float*>(smem + sl.ring);
   StageDesc* desc = reinterpret_cast<StageDesc*>(smem + sl.desc);
-  uint64_t* inboxes[2] = {reinterpret_cast<uint64_t*>(smem + sl.inbox0),
-                          reinterpret_cast<uint64_t*>(smem + sl.inbox1)};
+  uint64_t* const inbox0 = reinterpret_cast<uint64_t*>(smem + sl.inbox0);
+  uint64_t* const inbox1 = reinterpret_cast<uint64_t*>(smem + sl.inbox1);
   uint64_t* tray = reinterpret_cast<uint64_t*>(smem + sl.tray);
   uint64_t* kept = reinterpret_cast<uint64_t*>(smem + sl.kept);
   uint32_t* perm = reinterpret_cast<uint32_t*>(smem + sl.perm);
@@ -684,8 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
 
   for (int j = tid; j < kp; j += kThreads) kept[j] = 0ull;
   for (int j = tid; j < kInbox; j += kThreads) {
-    inboxes[0][j] = 0ull;
-    inboxes[1][j] = 0ull;
+    inbox0[j] = 0ull;
+    inbox1[j] = 0ull;
   }
   if (tid == 0) {
     for (int q = 0; q < 2; ++q) {
@@ -977,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             }
             __nanosleep(64);
           }
-          volatile uint64_t* ib = inboxes[par];
+          volatile uint64_t* ib = par ? inbox1 : inbox0;
           if (clean) {
             for (uint32_t mm = passm; mm; mm &= mm - 1u) {
               const int e = __ffs(mm) - 1;
@@ -1031,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   int kept_n = 0;       // real words in the kept list
   int pruned = 0;       // tray words left by the last prune
   uint64_t theta = 0ull;
-  uint32_t head[2] = {0u, 0u};
+  uint32_t head = 0, head_other = 0;  // inbox heads: this piece's parity, the other one
   int par = 0;
   int warm_next = 0;  // next piece whose starting threshold is to be set
   const int m_warm = (k + kNS - 1) / kNS;
@@ -1054,11 +1067,34 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       // every reader observes the copy's completion itself (already complete)
       if (!mbar_wait(&full[slot], (g / uint32_t(nstage)) & 1u, kWaitLimit)) timed_out = true;
       const StageDesc d = desc[slot];
-      float x[kEPT];
-      const uint32_t valid = load_share(x, ring + slot * kUnit, wrow, d.e0, d.nvalid,
-                                        waligned ? (d.nvalid & ~3u) : 0u, stt);
-      if (m_warm <= 64) top.add(x, valid);
-      else est = warp_key_bound(x, valid, m_warm);
+      const float* src = ring + slot * kUnit;
+      const uint32_t copied = waligned ? (d.nvalid & ~3u) : 0u;
+      if (m_warm <= 64) {
+        // streamed a float4 at a time: nothing but the lane's list stays live
+        if (copied == uint32_t(kUnit)) {
+#pragma unroll 2
+          for (int u = 0; u < kF4; ++u) {
+            const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
+            top.add_value(v.x);
+            top.add_value(v.y);
+            top.add_value(v.z);
+            top.add_value(v.w);
+          }
+        } else {
+          for (int u = 0; u < kF4; ++u) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t pos = uint32_t(4 * (stt + kNST * u) + c);
+              if (pos < copied) top.add_value(src[pos]);
+              else if (pos < d.nvalid) top.add_value(__ldg(wrow + d.e0 + pos));
+            }
+          }
+        }
+      } else {
+        float x[kEPT];
+        const uint32_t valid = load_share(x, src, wrow, d.e0, d.nvalid, copied, stt);
+        est = warp_key_bound(x, valid, m_warm);
+      }
     }
     if (m_warm <= 64) est = top.bound(m_warm);
     if (lane == 0) st.est[swarp] = est;
@@ -1222,8 +1258,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   // Move `n` reserved words of inbox `par` into the tray (a slot still 0 is
   // reserved but not yet written: wait for it), and free their slots.
   auto take = [&](int n) {
-    volatile uint64_t* ib = inboxes[par];
-    const uint32_t h = head[par];
+    volatile uint64_t* ib = par ? inbox1 : inbox0;
+    const uint32_t h = head;
     for (int j = stt; j < n; j += kNST) {
       volatile uint64_t* slot = ib + ((h + uint32_t(j)) & (kInbox - 1));
       uint64_t w = *slot;
@@ -1241,9 +1277,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     }
     __threadfence_block();  // the emptied slots are visible before head moves
     Sel::sync();
-    head[par] = h + uint32_t(n);
+    head = h + uint32_t(n);
     tray_n += n;
-    if (stt == 0) *reinterpret_cast<volatile uint32_t*>(&st.head[par]) = head[par];
+    if (stt == 0) *reinterpret_cast<volatile uint32_t*>(&st.head[par]) = head;
   };
 
   for (int j = 0;; ++j) {
@@ -1274,6 +1310,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     Sel::sync();
     if (!have) break;
     par = j & 1;
+    if (j > 0) {  // pieces alternate inboxes: pick up this parity's head
+      const uint32_t h = head;
+      head = head_other;
+      head_other = h;
+    }
     const int fd_target = kNF * (j / 2 + 1);
 
     for (;;) {
@@ -1315,7 +1356,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           }
           const int fd = *reinterpret_cast<volatile int*>(&st.fdone[par]);
           const uint32_t tail = *reinterpret_cast<volatile uint32_t*>(&st.tail[par]);
-          const uint32_t avail = tail - head[par];
+          const uint32_t avail = tail - head;
           n = int(min(avail, uint32_t(kTray - tray_n)));
           if (n > kTakeMax) n = kTakeMax;
           if (fd < fd_target && avail < uint32_t(kTakeMin)) n = 0;
@@ -1385,7 +1426,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         // Gather lists into this piece's (drained) inbox + the tray and merge
         // them as a tree of parallel pairwise merges; the running result
         // stays in slot 0.
-        uint64_t* slots = par == 0 ? inboxes[0] : tray;  // kInbox + kTray contiguous words
+        uint64_t* slots = par == 0 ? inbox0 : tray;  // kInbox + kTray contiguous words
         const int cap = (kInbox + kTray) / kp;
         for (int q = stt; q < kp; q += kNST) slots[q] = kept[q];
         int next_other = 0;  // next contributor to gather (never this CTA)
@@ -1431,7 +1472,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         }
         write_row(p, pc.r, slots, stt, kNST);
         Sel::sync();
-        for (int q = stt; q < kInbox; q += kNST) inboxes[par][q] = 0ull;  // empty slots again
+        uint64_t* ib = par ? inbox1 : inbox0;
+        for (int q = stt; q < kInbox; q += kNST) ib[q] = 0ull;  // empty slots again
         __threadfence_block();
         if (stt == 0) {
           p.row_theta[pc.r] = 0ull;
