@@ -52,6 +52,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// Bounded wait that sleeps `ns` nanoseconds between polls, so that a warp
+// waiting for a long time leaves the issue slots of its SM sub-partition to
+// the warps that have work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t limit,
+                                                unsigned ns) {
+  for (uint32_t it = 0; it < limit; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(ns);
+  }
+  return false;
+}
+
 // Bulk copy global -> this CTA's shared memory, completing on `bar`.  Both
 // addresses 16-byte aligned, `bytes` a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

@@ -312,6 +312,8 @@ struct CtaState {
   int sel_b, sel_above, sel_binc;  // histogram select: chosen bin and counts
   int sel_n, sel_done;             // selector step: words to take, piece done
   uint32_t est[kNS];               // warm start: per selector warp key bound
+  uint32_t est2[kNS];              // warm start: per selector warp candidate bound
+  uint32_t warm_cnt;               // warm start: elements reaching the candidate
   int warm_pub;                    // pieces whose starting threshold is set
   int first_issued;                // pieces whose first stage the producer has issued
   unsigned long long theta[2];     // threshold word of the piece using inbox p
@@ -589,15 +591,17 @@ __device__ __forceinline__ uint32_t share_key(const float (&x)[kEPT], uint32_t v
 }
 
 // For m <= 64 the counts run over the union of every lane's four largest
-// keys (128 values per warp): T is reached by at least m real elements, and
-// falls short of the exact bound only when some lane holds more than four
-// of the warp's top m.  Lane lists are kept sorted, l0 >= l1 >= l2 >= l3.
+// keys of one unit (128 values per warp): T is reached by at least m real
+// elements, and falls short of the exact bound only when some lane holds
+// more than four of the warp's top m.  Lane lists are kept sorted,
+// l0 >= l1 >= l2 >= l3; padding and NaN have key 0 and never count.
 struct Top4 {
   uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;
-  uint32_t real = 0;  // valid, non-NaN elements seen by this lane
-  // one element (key 0: padding or NaN)
+  static __device__ __forceinline__ uint32_t key_of(float x) {
+    const uint32_t bits = __float_as_uint(x);
+    return (bits & 0x7FFFFFFFu) <= 0x7F800000u ? order_key(bits) : 0u;
+  }
   __device__ __forceinline__ void add(uint32_t v) {
-    real += v != 0u ? 1u : 0u;
     const uint32_t a3 = max(l3, min(l2, v));
     const uint32_t a2 = max(l2, min(l1, v));
     const uint32_t a1 = max(l1, min(l0, v));
@@ -606,30 +610,64 @@ struct Top4 {
     l2 = a2;
     l3 = a3;
   }
-  __device__ __forceinline__ void add_value(float x) {
-    const uint32_t bits = __float_as_uint(x);
-    add((bits & 0x7FFFFFFFu) <= 0x7F800000u ? order_key(bits) : 0u);
+  // four elements: sort them (five compare-exchanges), then the top four of
+  // both sorted lists are max(l_i, g_{3-i}), a bitonic sequence that two
+  // rounds of compare-exchanges sort
+  __device__ __forceinline__ void add4(float4 f) {
+    uint32_t a = key_of(f.x), b = key_of(f.y), c = key_of(f.z), d = key_of(f.w);
+    auto cx = [](uint32_t& x, uint32_t& y) {
+      const uint32_t hi = max(x, y), lo = min(x, y);
+      x = hi;
+      y = lo;
+    };
+    cx(a, b);
+    cx(c, d);
+    cx(a, c);
+    cx(b, d);
+    cx(b, c);
+    uint32_t m0 = max(l0, d), m1 = max(l1, c), m2 = max(l2, b), m3 = max(l3, a);
+    cx(m0, m2);
+    cx(m1, m3);
+    cx(m0, m1);
+    cx(m2, m3);
+    l0 = m0;
+    l1 = m1;
+    l2 = m2;
+    l3 = m3;
+  }
+  __device__ __forceinline__ uint32_t count_ge(uint32_t t) const {
+    return (l0 >= t ? 1u : 0u) + (l1 >= t ? 1u : 0u) + (l2 >= t ? 1u : 0u) + (l3 >= t ? 1u : 0u);
   }
   __device__ __forceinline__ uint32_t bound(int m) const {
-    if (__reduce_add_sync(0xFFFFFFFFu, real) < uint32_t(m)) return 0u;
-    const uint32_t mm = uint32_t(m);
-    uint32_t T = 0;
+    uint32_t T1, T2;
+    bound2(m, m, T1, T2);
+    return T1;
+  }
+  // Two searches at once (targets m1, m2), six trial keys per step, their
+  // counts packed into two reductions.
+  __device__ __forceinline__ void bound2(int m1, int m2, uint32_t& T1, uint32_t& T2) const {
+    const uint32_t mm1 = uint32_t(m1), mm2 = uint32_t(m2);
+    T1 = 0;
+    T2 = 0;
 #pragma unroll 1
     for (int b = 31; b >= 17; b -= 2) {
-      uint32_t pk = 0;  // three counts of at most 128, eight bits each
+      uint32_t pk1 = 0, pk2 = 0;  // three counts of at most 128 each, eight bits each
 #pragma unroll
       for (uint32_t i = 1; i <= 3; ++i) {
-        const uint32_t t = T | (i << (b - 1));
-        pk += ((l0 >= t ? 1u : 0u) + (l1 >= t ? 1u : 0u) + (l2 >= t ? 1u : 0u) +
-               (l3 >= t ? 1u : 0u)) << (8 * (i - 1));
+        pk1 += count_ge(T1 | (i << (b - 1))) << (8 * (i - 1));
+        pk2 += count_ge(T2 | (i << (b - 1))) << (8 * (i - 1));
       }
-      pk = __reduce_add_sync(0xFFFFFFFFu, pk);
-      const uint32_t i = ((pk >> 16) & 0xFFu) >= mm ? 3u
-                         : ((pk >> 8) & 0xFFu) >= mm ? 2u
-                         : (pk & 0xFFu) >= mm ? 1u : 0u;
-      T |= i << (b - 1);
+      pk1 = __reduce_add_sync(0xFFFFFFFFu, pk1);
+      pk2 = __reduce_add_sync(0xFFFFFFFFu, pk2);
+      const uint32_t i1 = ((pk1 >> 16) & 0xFFu) >= mm1 ? 3u
+                          : ((pk1 >> 8) & 0xFFu) >= mm1 ? 2u
+                          : (pk1 & 0xFFu) >= mm1 ? 1u : 0u;
+      const uint32_t i2 = ((pk2 >> 16) & 0xFFu) >= mm2 ? 3u
+                          : ((pk2 >> 8) & 0xFFu) >= mm2 ? 2u
+                          : (pk2 & 0xFFu) >= mm2 ? 1u : 0u;
+      T1 |= i1 << (b - 1);
+      T2 |= i2 << (b - 1);
     }
-    return T;
   }
 };
 
@@ -668,6 +706,142 @@ __host__ __device__ inline int warm_units(int k, int nu) {
   const int m = (k + kNS - 1) / kNS;
   if (m > 64) return 1;
   return nu < 1 ? 1 : (nu < kWarmUnits ? nu : kWarmUnits);
+}
+
+// Warm start of piece w, whose first units have landed in the ring (the
+// filters hold them until the threshold is set), run by the selector team:
+// each selector warp bounds its share of those units, the smallest bound is
+// reached by at least k elements of the piece.  The piece may use the
+// threshold word of its parity: the piece before it in that parity is
+// finished.  A function of its own (not inlined), so that the lane lists
+// keep registers instead of competing with the selector loop's state.
+// Returns false if a wait gave up.
+__device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_stride,
+                                              unsigned long long* row_theta, CtaState& st,
+                                              int w, const float* ring, const StageDesc* desc,
+                                              uint64_t* full, int nstage, int k, int stt) {
+  using Sel = Team<kNST, 1>;
+  const int lane = stt & 31, swarp = stt >> 5;
+  const int m_warm = (k + kNS - 1) / kNS;
+  bool ok = true;
+  const Piece pw = st.table[w % kTable];
+  const int wu = warm_units(k, pw.u_end - pw.u_begin);
+  const float* wrow = scores + int64_t(pw.r) * row_stride;
+  const bool waligned = (reinterpret_cast<uintptr_t>(wrow) & 15u) == 0;
+  auto stage_of = [&](int q, const float*& src, StageDesc& d, uint32_t& copied) {
+    const uint32_t g = pw.g_first + uint32_t(q);
+    const int slot = int(g % uint32_t(nstage));
+    // every reader observes the copy's completion itself (already complete)
+    if (!mbar_wait(&full[slot], (g / uint32_t(nstage)) & 1u, kWaitLimit)) ok = false;
+    d = desc[slot];
+    src = ring + slot * kUnit;
+    copied = waligned ? (d.nvalid & ~3u) : 0u;
+  };
+  if (stt == 0) st.warm_cnt = 0u;
+  uint32_t mk;
+  if (m_warm > 64) {
+    // one unit, all 32 keys of every lane
+    const float* src;
+    StageDesc d;
+    uint32_t copied;
+    stage_of(0, src, d, copied);
+    float x[kEPT];
+    const uint32_t valid = load_share(x, src, wrow, d.e0, d.nvalid, copied, stt);
+    const uint32_t est = warp_key_bound(x, valid, m_warm);
+    if (lane == 0) st.est[swarp] = est;
+    Sel::sync();
+    mk = 0xFFFFFFFFu;
+#pragma unroll
+    for (int q = 0; q < kNS; ++q) mk = min(mk, st.est[q]);
+  } else {
+    // Lane lists of the first unit give two bounds per warp: a safe one
+    // (m elements of the unit) and a candidate for all wu units (about
+    // 1.25 m / wu elements of the unit).  The candidate is taken if a count
+    // finds k elements at or above it: the lane lists' count in the first
+    // unit (a lower bound) plus a strict float compare over the other units
+    // (it never counts NaN, and misses only -0.0 against a +0.0 bound).
+    Top4 top;
+    {
+      const float* src;
+      StageDesc d;
+      uint32_t copied;
+      stage_of(0, src, d, copied);
+      if (copied == uint32_t(kUnit)) {
+#pragma unroll 2
+        for (int u = 0; u < kF4; ++u) top.add4(reinterpret_cast<const float4*>(src)[stt + kNST * u]);
+      } else {
+        for (int u = 0; u < kF4; ++u) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t pos = uint32_t(4 * (stt + kNST * u) + c);
+            if (pos < copied) top.add(Top4::key_of(src[pos]));
+            else if (pos < d.nvalid) top.add(Top4::key_of(__ldg(wrow + d.e0 + pos)));
+          }
+        }
+      }
+    }
+    const int m_c = wu > 1 ? (5 * m_warm + 4 * wu - 1) / (4 * wu) : m_warm;
+    uint32_t es, ec;
+    top.bound2(m_warm, m_c, es, ec);
+    if (lane == 0) {
+      st.est[swarp] = es;
+      st.est2[swarp] = ec;
+    }
+    Sel::sync();
+    uint32_t ms = 0xFFFFFFFFu, mc = 0xFFFFFFFFu;
+#pragma unroll
+    for (int q = 0; q < kNS; ++q) {
+      ms = min(ms, st.est[q]);
+      mc = min(mc, st.est2[q]);
+    }
+    mk = ms;
+    if (wu > 1 && mc > ms) {
+      uint32_t c = top.count_ge(mc);
+      const float flo = key_to_float(mc - 1u);  // key >= mc  <=>  value > flo
+      for (int q = 1; q < wu; ++q) {
+        const float* src;
+        StageDesc d;
+        uint32_t copied;
+        stage_of(q, src, d, copied);
+        if (copied == uint32_t(kUnit)) {
+#pragma unroll 4
+          for (int u = 0; u < kF4; ++u) {
+            const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
+            c += (v.x > flo ? 1u : 0u) + (v.y > flo ? 1u : 0u) + (v.z > flo ? 1u : 0u) +
+                 (v.w > flo ? 1u : 0u);
+          }
+        } else {
+          for (int u = 0; u < kF4; ++u) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const uint32_t pos = uint32_t(4 * (stt + kNST * u) + cc);
+              float v = -__int_as_float(0x7F800000);
+              if (pos < copied) v = src[pos];
+              else if (pos < d.nvalid) v = __ldg(wrow + d.e0 + pos);
+              c += v > flo ? 1u : 0u;
+            }
+          }
+        }
+      }
+      c = __reduce_add_sync(0xFFFFFFFFu, c);
+      if (lane == 0) atomicAdd(&st.warm_cnt, c);
+      Sel::sync();
+      if (st.warm_cnt >= uint32_t(k)) mk = mc;
+    }
+  }
+  if (stt == 0) {
+    const uint64_t th0 = mk ? (uint64_t(mk) << 32) - 1ull : 0ull;
+    if (th0) {
+      // shared with the row's other CTAs without waiting for the reply (the
+      // selector loop reads their thresholds back)
+      if (pw.contributors > 1) atomicMax(&row_theta[pw.r], (unsigned long long)th0);
+      atomicMax(&st.theta[w & 1], (unsigned long long)th0);
+    }
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(&st.warm_pub) = w + 1;
+  }
+  Sel::sync();  // the bounds are read before the next warm start rewrites them
+  return ok;
 }
 
 // ---------------------------------------------------------------------------
@@ -732,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     // wait for ring slot `stage` to be free, then hand it a descriptor
     auto next_slot = [&]() {
       if (g >= uint32_t(nstage) &&
-          !mbar_wait(&empty[stage], phase ^ 1u, gave_up ? 1u : kWaitLimit))
+          !mbar_wait_sleep(&empty[stage], phase ^ 1u, gave_up ? 1u : kWaitLimit, 64))
         gave_up = true;
     };
     auto advance = [&]() {
@@ -868,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     // every exit decision is warp-uniform: a wait that gave up in any lane
     // ends the warp's loop
     for (;;) {
-      if (!mbar_wait(&full[stage], phase, kWaitLimit)) timed_out = true;
+      if (!mbar_wait_sleep(&full[stage], phase, kWaitLimit, 32)) timed_out = true;
       const StageDesc d = desc[stage];
       if (__any_sync(0xFFFFFFFFu, timed_out)) {
         timed_out = true;
@@ -888,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               timed_out = true;
               break;
             }
-            __nanosleep(32);
+            __nanosleep(200);
           }
         }
         if (__any_sync(0xFFFFFFFFu, timed_out)) {
@@ -1047,88 +1221,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   uint32_t head = 0, head_other = 0;  // inbox heads: this piece's parity, the other one
   int par = 0;
   int warm_next = 0;  // next piece whose starting threshold is to be set
-  const int m_warm = (k + kNS - 1) / kNS;
-
-  // Warm start of piece w, whose first units have landed in the ring (the
-  // filters hold them until the threshold is set): each selector warp bounds
-  // its share of those units, the smallest bound is reached by at least k
-  // elements of the piece.  The piece may use the threshold word of its
-  // parity: the piece before it in that parity is finished.
-  auto warm_start = [&](int w) {
-    const Piece pw = st.table[w % kTable];
-    const int wu = warm_units(k, pw.u_end - pw.u_begin);
-    const float* wrow = p.scores + int64_t(pw.r) * p.row_stride;
-    const bool waligned = (reinterpret_cast<uintptr_t>(wrow) & 15u) == 0;
-    uint32_t est = 0;
-    Top4 top;
-    for (int q = 0; q < wu; ++q) {
-      const uint32_t g = pw.g_first + uint32_t(q);
-      const int slot = int(g % uint32_t(nstage));
-      // every reader observes the copy's completion itself (already complete)
-      if (!mbar_wait(&full[slot], (g / uint32_t(nstage)) & 1u, kWaitLimit)) timed_out = true;
-      const StageDesc d = desc[slot];
-      const float* src = ring + slot * kUnit;
-      const uint32_t copied = waligned ? (d.nvalid & ~3u) : 0u;
-      if (m_warm <= 64) {
-        // streamed a float4 at a time: nothing but the lane's list stays live
-        if (copied == uint32_t(kUnit)) {
-#pragma unroll 2
-          for (int u = 0; u < kF4; ++u) {
-            const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
-            top.add_value(v.x);
-            top.add_value(v.y);
-            top.add_value(v.z);
-            top.add_value(v.w);
-          }
-        } else {
-          for (int u = 0; u < kF4; ++u) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint32_t pos = uint32_t(4 * (stt + kNST * u) + c);
-              if (pos < copied) top.add_value(src[pos]);
-              else if (pos < d.nvalid) top.add_value(__ldg(wrow + d.e0 + pos));
-            }
-          }
-        }
-      } else {
-        float x[kEPT];
-        const uint32_t valid = load_share(x, src, wrow, d.e0, d.nvalid, copied, stt);
-        est = warp_key_bound(x, valid, m_warm);
-      }
-    }
-    if (m_warm <= 64) est = top.bound(m_warm);
-    if (lane == 0) st.est[swarp] = est;
-    Sel::sync();
-    uint32_t mk = 0xFFFFFFFFu;
-#pragma unroll
-    for (int q = 0; q < kNS; ++q) mk = min(mk, st.est[q]);
-    if (stt == 0) {
-      const uint64_t th0 = mk ? (uint64_t(mk) << 32) - 1ull : 0ull;
-      if (th0) {
-        unsigned long long t = th0;
-        if (pw.contributors > 1) {
-          const unsigned long long old = atomicMax(&p.row_theta[pw.r], t);
-          if (old > t) t = old;
-        }
-        atomicMax(&st.theta[w & 1], t);
-      }
-      __threadfence_block();
-      *reinterpret_cast<volatile int*>(&st.warm_pub) = w + 1;
-    }
-    Sel::sync();  // the bounds are read before the next warm start rewrites them
-  };
 
   // Publish a threshold to the filters (and to the row's other CTAs).
   auto raise_theta = [&](uint64_t nth, const Piece& pc) {
     if (nth <= theta) return;
     theta = nth;
     if (stt == 0) {
-      unsigned long long t = nth;
-      if (pc.contributors > 1) {
-        const unsigned long long old = atomicMax(&p.row_theta[pc.r], t);
-        if (old > t) t = old;
-      }
-      atomicMax(&st.theta[par], t);
+      // shared with the row's other CTAs without waiting for the reply (the
+      // selector loop reads their thresholds back)
+      if (pc.contributors > 1) atomicMax(&p.row_theta[pc.r], (unsigned long long)nth);
+      atomicMax(&st.theta[par], (unsigned long long)nth);
     }
   };
 
@@ -1345,9 +1447,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               break;
             }
             if (*reinterpret_cast<volatile int*>(&st.first_issued) > warm_next) {
-              const uint32_t gl =
-                  pn.g_first + uint32_t(warm_units(k, pn.u_end - pn.u_begin) - 1);
-              if (mbar_try_wait(&full[gl % uint32_t(nstage)], (gl / uint32_t(nstage)) & 1u)) {
+              // copies can land out of order: every warm-start unit must be in
+              const int wu = warm_units(k, pn.u_end - pn.u_begin);
+              bool landed = true;
+              for (int q = 0; q < wu && landed; ++q) {
+                const uint32_t g = pn.g_first + uint32_t(q);
+                landed = mbar_try_wait(&full[g % uint32_t(nstage)], (g / uint32_t(nstage)) & 1u);
+              }
+              if (landed) {
                 warm = 1;
                 break;
               }
@@ -1389,7 +1496,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (sth > theta) theta = sth;
       Sel::sync();
       if (warm) {
-        if (warm == 1) warm_start(warm_next);
+        if (warm == 1 && !warm_start_piece(p.scores, p.row_stride, p.row_theta, st, warm_next, ring,
+                                           desc, full, nstage, k, stt))
+          timed_out = true;
         ++warm_next;
         continue;
       }
