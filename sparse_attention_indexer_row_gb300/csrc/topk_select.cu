@@ -1117,38 +1117,26 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         }
         uint32_t passm = ((g0 | g1) | (g2 | g3)) & valid;
         const uint32_t rare = ((q0 | q1) | (q2 | q3)) & valid;
-        // On a full stage the values are re-read from the stage (not released
-        // yet); a ragged stage has them in registers and takes a fixed walk.
-        // Then each lane with survivors reserves its own run of inbox slots
-        // (one shared-memory atomicAdd) and writes them.
-        const bool clean = copied == uint32_t(kUnit);
+        // The flagged values are re-read where they sit (the stage is not
+        // released yet); each lane with survivors reserves its own run of
+        // inbox slots (one shared-memory atomicAdd) and writes them.
         auto word_of = [&](uint32_t bits, int e) -> uint64_t {
           const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
           return (uint64_t(order_key(bits)) << 32) | uint64_t(~(e0 + pos));
         };
-        auto smem_bits = [&](int e) -> uint32_t {
-          return __float_as_uint(src[4 * (ft + kNFT * (e >> 2)) + (e & 3)]);
+        // an element's bits, re-read: from the stage, or past the copied
+        // prefix of a ragged unit from global memory (rare)
+        auto elem_bits = [&](int e) -> uint32_t {
+          const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
+          if (pos < copied) return __float_as_uint(src[pos]);
+          return __float_as_uint(__ldg(row + e0 + pos));
         };
-        if (rare) {
-          if (clean) {
-            for (uint32_t mm = rare; mm; mm &= mm - 1u) {
-              const int e = __ffs(mm) - 1;
-              const uint32_t bits = smem_bits(e);
-              const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
-              saw_nan |= nan;
-              if (!nan && word_of(bits, e) > th) passm |= 1u << e;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < kEPT; ++e) {
-              if ((rare >> e) & 1u) {
-                const uint32_t bits = __float_as_uint(x[e]);
-                const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
-                saw_nan |= nan;
-                if (!nan && word_of(bits, e) > th) passm |= 1u << e;
-              }
-            }
-          }
+        for (uint32_t mm = rare; mm; mm &= mm - 1u) {
+          const int e = __ffs(mm) - 1;
+          const uint32_t bits = elem_bits(e);
+          const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+          saw_nan |= nan;
+          if (!nan && word_of(bits, e) > th) passm |= 1u << e;
         }
         const uint32_t np = __popc(passm);
         if (np) {
@@ -1165,20 +1153,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             __nanosleep(64);
           }
           volatile uint64_t* ib = par ? inbox1 : inbox0;
-          if (clean) {
-            for (uint32_t mm = passm; mm; mm &= mm - 1u) {
-              const int e = __ffs(mm) - 1;
-              ib[pos & (kInbox - 1)] = word_of(smem_bits(e), e);
-              ++pos;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < kEPT; ++e) {
-              if ((passm >> e) & 1u) {
-                ib[pos & (kInbox - 1)] = word_of(__float_as_uint(x[e]), e);
-                ++pos;
-              }
-            }
+          for (uint32_t mm = passm; mm; mm &= mm - 1u) {
+            const int e = __ffs(mm) - 1;
+            ib[pos & (kInbox - 1)] = word_of(elem_bits(e), e);
+            ++pos;
           }
         }
       }
@@ -1447,10 +1425,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               break;
             }
             if (*reinterpret_cast<volatile int*>(&st.first_issued) > warm_next) {
-              // copies can land out of order: every warm-start unit must be in
+              // Copies can land out of order: for the next piece every
+              // warm-start unit must be in (the warm start must not block
+              // while this piece's inbox still needs draining).  For the
+              // current piece the filters have finished everything before
+              // it, so the producer can land the remaining units while the
+              // warm start works on the first one: it starts once that one
+              // is in.
               const int wu = warm_units(k, pn.u_end - pn.u_begin);
+              const int need = warm_next == j ? 1 : wu;
               bool landed = true;
-              for (int q = 0; q < wu && landed; ++q) {
+              for (int q = 0; q < need && landed; ++q) {
                 const uint32_t g = pn.g_first + uint32_t(q);
                 landed = mbar_try_wait(&full[g % uint32_t(nstage)], (g / uint32_t(nstage)) & 1u);
               }
