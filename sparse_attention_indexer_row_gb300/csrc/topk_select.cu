@@ -104,7 +104,7 @@ constexpr uint32_t kWaitLimit = 1u << 22;    // polls before a wait gives up
 // Launch plan, tuned for GB300's 152 SMs (results never depend on it).
 constexpr int kSms = 152;
 constexpr int kMaxFlatCtas = 256;  // persistent grid cap (workspace slots)
-constexpr int kMinFlatUnits = 4;   // at least 128 KB per persistent CTA
+constexpr int kMinFlatUnits = 16;  // a row is split into shares of at least 512 KB
 constexpr int kMinSegUnits = 4;    // at least 128 KB per split segment
 constexpr int kManyRows = kSms;    // rows per call from which rows are not split
 
@@ -1780,10 +1780,13 @@ int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_str
   int64_t G;
   const bool flat = split == 0 && lengths_or_null == nullptr && rows < kManyRows;
   if (flat) {
-    // one CTA per SM, equal shares of the batch's units
+    // one CTA per SM, equal shares of the batch's units: at least one CTA
+    // per row, and rows split only into shares of kMinFlatUnits or more
+    // (a split row ends in a leader merge of its CTAs' lists)
     const int64_t M = int64_t(rows) * u_full;
     G = cap;
-    const int64_t by_len = (M + kMinFlatUnits - 1) / kMinFlatUnits;
+    int64_t by_len = (M + kMinFlatUnits - 1) / kMinFlatUnits;
+    if (by_len < rows) by_len = rows;
     if (G > by_len) G = by_len;
     p.plan = kPlanFlat;
     p.split = 1;
