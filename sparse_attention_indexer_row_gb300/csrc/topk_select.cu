@@ -1086,58 +1086,56 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       const uint32_t copied = aligned ? (nvalid & ~3u) : 0u;
       float x[kEPT];
       const uint32_t valid = load_share(x, src, row, e0, nvalid, copied, ft);  // bit e: in the row
-      // Most stages have no element past the threshold: one chained float
-      // test first (a superset: it also passes NaN, ties and padding), the
-      // per-element mask only when some lane needs it.
-      // (four independent chains keep the test short in latency)
-      bool m0 = false, m1 = false, m2 = false, m3 = false;
+      // Most stages have no element past the threshold: the test first folds
+      // each float4 group into one bit (a superset: it also passes NaN, ties
+      // and padding); only flagged groups are re-read (where they sit: the
+      // stage is not released yet, or past the copied prefix of a ragged
+      // unit, global memory) and classified element by element.
+      uint32_t gm = 0;  // bit u: group u (elements 4u .. 4u+3) may hold a survivor
 #pragma unroll
-      for (int u = 0; u < kF4; ++u) {
-        m0 |= !(x[4 * u + 0] < thf);
-        m1 |= !(x[4 * u + 1] < thf);
-        m2 |= !(x[4 * u + 2] < thf);
-        m3 |= !(x[4 * u + 3] < thf);
-      }
-      if (__any_sync(0xFFFFFFFFu, (m0 | m1) | (m2 | m3))) {
+      for (int u = 0; u < kF4; ++u)
+        gm |= uint32_t(!(x[4 * u + 0] < thf) | !(x[4 * u + 1] < thf) | !(x[4 * u + 2] < thf) |
+                       !(x[4 * u + 3] < thf)) << u;
+      auto word_of = [&](uint32_t bits, int e) -> uint64_t {
+        const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
+        return (uint64_t(order_key(bits)) << 32) | uint64_t(~(e0 + pos));
+      };
+      auto elem_bits = [&](int e) -> uint32_t {
+        const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
+        if (pos < copied) return __float_as_uint(src[pos]);
+        return __float_as_uint(__ldg(row + e0 + pos));
+      };
+      if (__any_sync(0xFFFFFFFFu, gm != 0u)) {
         // A strict float compare is already the exact word test for every
         // value except NaN and values equal to the threshold's own (ties,
         // and -0.0 against +0.0): those few get the 64-bit word test.
-        uint32_t g0 = 0, g1 = 0, g2 = 0, g3 = 0;  // bit e: x[e] > the threshold value
-        uint32_t q0 = 0, q1 = 0, q2 = 0, q3 = 0;  // bit e: x[e] equal to it, or NaN
+        uint32_t passm = 0;
+        for (uint32_t gg = gm; gg; gg &= gg - 1u) {
+          const int u = __ffs(gg) - 1;
+          float4 v;
+          if (copied == uint32_t(kUnit)) {
+            v = reinterpret_cast<const float4*>(src)[ft + kNFT * u];
+          } else {
+            v.x = __uint_as_float(((valid >> (4 * u + 0)) & 1u) ? elem_bits(4 * u + 0) : 0u);
+            v.y = __uint_as_float(((valid >> (4 * u + 1)) & 1u) ? elem_bits(4 * u + 1) : 0u);
+            v.z = __uint_as_float(((valid >> (4 * u + 2)) & 1u) ? elem_bits(4 * u + 2) : 0u);
+            v.w = __uint_as_float(((valid >> (4 * u + 3)) & 1u) ? elem_bits(4 * u + 3) : 0u);
+          }
+          const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int u = 0; u < kF4; ++u) {
-          g0 |= uint32_t(x[4 * u + 0] > thf) << (4 * u + 0);
-          g1 |= uint32_t(x[4 * u + 1] > thf) << (4 * u + 1);
-          g2 |= uint32_t(x[4 * u + 2] > thf) << (4 * u + 2);
-          g3 |= uint32_t(x[4 * u + 3] > thf) << (4 * u + 3);
-          q0 |= uint32_t(!(x[4 * u + 0] < thf) && !(x[4 * u + 0] > thf)) << (4 * u + 0);
-          q1 |= uint32_t(!(x[4 * u + 1] < thf) && !(x[4 * u + 1] > thf)) << (4 * u + 1);
-          q2 |= uint32_t(!(x[4 * u + 2] < thf) && !(x[4 * u + 2] > thf)) << (4 * u + 2);
-          q3 |= uint32_t(!(x[4 * u + 3] < thf) && !(x[4 * u + 3] > thf)) << (4 * u + 3);
+          for (int c = 0; c < 4; ++c) {
+            const int e = 4 * u + c;
+            bool pass = vv[c] > thf;
+            if (!(vv[c] < thf) && !pass) {  // equal to the threshold's value, or NaN
+              const uint32_t bits = __float_as_uint(vv[c]);
+              const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+              saw_nan |= nan && ((valid >> e) & 1u);
+              pass = !nan && word_of(bits, e) > th;
+            }
+            passm |= uint32_t(pass) << e;
+          }
         }
-        uint32_t passm = ((g0 | g1) | (g2 | g3)) & valid;
-        const uint32_t rare = ((q0 | q1) | (q2 | q3)) & valid;
-        // The flagged values are re-read where they sit (the stage is not
-        // released yet); each lane with survivors reserves its own run of
-        // inbox slots (one shared-memory atomicAdd) and writes them.
-        auto word_of = [&](uint32_t bits, int e) -> uint64_t {
-          const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
-          return (uint64_t(order_key(bits)) << 32) | uint64_t(~(e0 + pos));
-        };
-        // an element's bits, re-read: from the stage, or past the copied
-        // prefix of a ragged unit from global memory (rare)
-        auto elem_bits = [&](int e) -> uint32_t {
-          const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
-          if (pos < copied) return __float_as_uint(src[pos]);
-          return __float_as_uint(__ldg(row + e0 + pos));
-        };
-        for (uint32_t mm = rare; mm; mm &= mm - 1u) {
-          const int e = __ffs(mm) - 1;
-          const uint32_t bits = elem_bits(e);
-          const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
-          saw_nan |= nan;
-          if (!nan && word_of(bits, e) > th) passm |= 1u << e;
-        }
+        passm &= valid;
         const uint32_t np = __popc(passm);
         if (np) {
           uint32_t pos = atomicAdd(&st.tail[par], np);
