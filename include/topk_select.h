@@ -21,7 +21,10 @@
  * blocks visited in a seeded shuffled order), a bitonic sort that runs on the
  * tray only, and for short batches a split of
  * each row over several CTAs whose local winners a ticket-elected leader
- * merges (video transcript 3:18-5:45).
+ * merges (video transcript 3:18-5:45).  A long piece of a row may start from a
+ * threshold that a sample of its first units only makes likely; the row's
+ * result is checked against it at the end and, if fewer than k scores of the
+ * row lie above it, the row is selected again (TOPK_STATUS_RESCAN).
  *
  * Memory: every pointer argument is caller-owned.  The library allocates no
  * memory, frees none, keeps no device state between calls and never
@@ -61,6 +64,10 @@ extern "C" {
 #define TOPK_STATUS_BAD_LENGTH 2u /* lengths[r] outside [0, n]; clamped */
 #define TOPK_STATUS_TIMEOUT 4u    /* a bounded wait on a bulk copy gave up; the
                                      affected rows' outputs are unspecified */
+#define TOPK_STATUS_RESCAN 8u     /* information only: some row's speculative
+                                     starting threshold left fewer than k of its
+                                     scores above it, and the row was selected
+                                     again from global memory (results exact) */
 
 /* Flags for topk_select_ex. */
 #define TOPK_FLAG_IDENTITY_ORDER 1u /* visit units in address order instead of

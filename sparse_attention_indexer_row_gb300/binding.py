@@ -24,6 +24,7 @@ TOPK_ERR_NOSPACE = 6
 TOPK_STATUS_NAN = 1
 TOPK_STATUS_BAD_LENGTH = 2
 TOPK_STATUS_TIMEOUT = 4
+TOPK_STATUS_RESCAN = 8
 TOPK_FLAG_IDENTITY_ORDER = 1
 TOPK_MAX_K = 2048
 

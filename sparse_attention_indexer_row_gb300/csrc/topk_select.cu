@@ -80,6 +80,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "device_util.cuh"
 #include "topk_select.h"
@@ -98,6 +99,13 @@ constexpr int kWarmUnits = 4;                // units a warm start reads (k <= 5
 // (k <= 512 runs a five-stage ring: the producer can land all warm-start
 // units of a piece while the filters hold its first one)
 static_assert(kWarmUnits <= 5, "warm-start units fit in the ring");
+// Speculative start: a piece of at least kSpecMinUnits units may start from a
+// threshold its warm-start units only make likely (about 3.6 k words of the
+// row above it).  It is taken when those units hold at least
+// 2.5 k * sample / row length elements at or above it, at most kSpecMaxNeed.
+constexpr int kSpecMinUnits = 16;
+constexpr uint32_t kSpecMaxNeed = 128;
+constexpr int kRescanChunk = 2048;           // row elements a rescan step reads
 constexpr int kMaxSplit = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls before a wait gives up
 
@@ -154,11 +162,13 @@ constexpr int kPlanFlat = 1;   // equal shares of the batch's units
 //                         (the three counters accumulate until read)
 //   theta     u64[rows]   split rows: best threshold word any of the row's CTAs
 //                         has reached, zero between calls
+//   spec      u64[rows]   split rows: largest speculative threshold word any of
+//                         the row's pieces started from, zero between calls
 //   partials  u64[slots][kp]  local top-k lists of split rows; slots =
 //                         max(rows * split, 2 * kMaxFlatCtas) when rows can
 //                         be split, else none
 struct WsLayout {
-  size_t tickets, survivors, sorts, admitted, theta, partials, total;
+  size_t tickets, survivors, sorts, admitted, theta, spec, partials, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -208,6 +218,8 @@ WsLayout ws_layout(int32_t rows, int32_t kp, size_t slots) {
   off = align256(off + sizeof(uint32_t) * size_t(rows));
   L.theta = off;
   off = align256(off + sizeof(uint64_t) * size_t(rows));
+  L.spec = off;
+  off = align256(off + sizeof(uint64_t) * size_t(rows));
   L.partials = off;
   off = align256(off + sizeof(uint64_t) * slots * size_t(kp));
   L.total = off;
@@ -238,6 +250,7 @@ struct Params {
   uint32_t* sorts;
   uint32_t* admitted;
   unsigned long long* row_theta;
+  unsigned long long* row_spec;
   uint64_t* partials;
   uint32_t seed_lo, seed_hi;
   uint32_t flags;
@@ -314,6 +327,9 @@ struct CtaState {
   uint32_t est[kNS];               // warm start: per selector warp key bound
   uint32_t est2[kNS];              // warm start: per selector warp candidate bound
   uint32_t warm_cnt;               // warm start: elements reaching the candidate
+  uint32_t est3[kNS];              // warm start: per selector warp largest key
+  uint32_t spec_cnt[2];            // warm start: sample counts of the speculative bounds
+  unsigned long long spec[2];      // speculative threshold word of the piece using inbox p
   int warm_pub;                    // pieces whose starting threshold is set
   int first_issued;                // pieces whose first stage the producer has issued
   unsigned long long theta[2];     // threshold word of the piece using inbox p
@@ -717,7 +733,8 @@ __host__ __device__ inline int warm_units(int k, int nu) {
 // keep registers instead of competing with the selector loop's state.
 // Returns false if a wait gave up.
 __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_stride,
-                                              unsigned long long* row_theta, CtaState& st,
+                                              unsigned long long* row_theta,
+                                              unsigned long long* row_spec, CtaState& st,
                                               int w, const float* ring, const StageDesc* desc,
                                               uint64_t* full, int nstage, int k, int stt) {
   using Sel = Team<kNST, 1>;
@@ -738,95 +755,215 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
     copied = waligned ? (d.nvalid & ~3u) : 0u;
   };
   if (stt == 0) st.warm_cnt = 0u;
-  uint32_t mk;
-  if (m_warm > 64) {
-    // one unit, all 32 keys of every lane
-    const float* src;
-    StageDesc d;
-    uint32_t copied;
-    stage_of(0, src, d, copied);
-    float x[kEPT];
-    const uint32_t valid = load_share(x, src, wrow, d.e0, d.nvalid, copied, stt);
-    const uint32_t est = warp_key_bound(x, valid, m_warm);
-    if (lane == 0) st.est[swarp] = est;
-    Sel::sync();
-    mk = 0xFFFFFFFFu;
-#pragma unroll
-    for (int q = 0; q < kNS; ++q) mk = min(mk, st.est[q]);
-  } else {
-    // Lane lists of the first unit give two bounds per warp: a safe one
-    // (m elements of the unit) and a candidate for all wu units (about
-    // 1.25 m / wu elements of the unit).  The candidate is taken if a count
-    // finds k elements at or above it: the lane lists' count in the first
-    // unit (a lower bound) plus a strict float compare over the other units
-    // (it never counts NaN, and misses only -0.0 against a +0.0 bound).
-    Top4 top;
-    {
-      const float* src;
-      StageDesc d;
-      uint32_t copied;
-      stage_of(0, src, d, copied);
-      if (copied == uint32_t(kUnit)) {
-#pragma unroll 2
-        for (int u = 0; u < kF4; ++u) top.add4(reinterpret_cast<const float4*>(src)[stt + kNST * u]);
-      } else {
-        for (int u = 0; u < kF4; ++u) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t pos = uint32_t(4 * (stt + kNST * u) + c);
-            if (pos < copied) top.add(Top4::key_of(src[pos]));
-            else if (pos < d.nvalid) top.add(Top4::key_of(__ldg(wrow + d.e0 + pos)));
-          }
-        }
-      }
-    }
-    const int m_c = wu > 1 ? (5 * m_warm + 4 * wu - 1) / (4 * wu) : m_warm;
-    uint32_t es, ec;
-    top.bound2(m_warm, m_c, es, ec);
-    if (lane == 0) {
-      st.est[swarp] = es;
-      st.est2[swarp] = ec;
-    }
-    Sel::sync();
-    uint32_t ms = 0xFFFFFFFFu, mc = 0xFFFFFFFFu;
-#pragma unroll
-    for (int q = 0; q < kNS; ++q) {
-      ms = min(ms, st.est[q]);
-      mc = min(mc, st.est2[q]);
-    }
-    mk = ms;
-    if (wu > 1 && mc > ms) {
-      uint32_t c = top.count_ge(mc);
-      const float flo = key_to_float(mc - 1u);  // key >= mc  <=>  value > flo
-      for (int q = 1; q < wu; ++q) {
+  uint32_t mk = 0u;
+  uint64_t spec = 0ull;  // speculative threshold word (0: none)
+  bool decided = false;
+  // Speculative start (long pieces, k <= 512): the 8th, 7th and 6th largest
+  // of the selector warps' largest keys in the first unit are candidates;
+  // the highest one that the wu sample units hold at least `need` elements
+  // at or above is taken (need = 2.5 k * sample / row length, so that the row
+  // holds about 3.6 k above it).  The count is a strict float compare (it
+  // never counts NaN, and misses only -0.0 against a +0.0 bound).  Only when
+  // no candidate is supported do the lane lists below run.
+  const int nu = pw.u_end - pw.u_begin;
+  if (m_warm <= 64 && wu == kWarmUnits && nu >= kSpecMinUnits) {
+    const uint64_t sample = uint64_t(wu) * uint64_t(kUnit);
+    const uint64_t need64 = (5ull * uint64_t(k) * sample + 2ull * pw.L - 1ull) / (2ull * pw.L);
+    if (need64 <= kSpecMaxNeed) {
+      const uint32_t need = uint32_t(need64);
+      float lm = -__int_as_float(0x7F800000);
+      {
         const float* src;
         StageDesc d;
         uint32_t copied;
-        stage_of(q, src, d, copied);
+        stage_of(0, src, d, copied);
         if (copied == uint32_t(kUnit)) {
-#pragma unroll 4
+#pragma unroll
           for (int u = 0; u < kF4; ++u) {
             const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
-            c += (v.x > flo ? 1u : 0u) + (v.y > flo ? 1u : 0u) + (v.z > flo ? 1u : 0u) +
-                 (v.w > flo ? 1u : 0u);
+            lm = fmaxf(lm, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
           }
         } else {
           for (int u = 0; u < kF4; ++u) {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const uint32_t pos = uint32_t(4 * (stt + kNST * u) + cc);
-              float v = -__int_as_float(0x7F800000);
-              if (pos < copied) v = src[pos];
-              else if (pos < d.nvalid) v = __ldg(wrow + d.e0 + pos);
-              c += v > flo ? 1u : 0u;
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t pos = uint32_t(4 * (stt + kNST * u) + c);
+              if (pos < copied) lm = fmaxf(lm, src[pos]);
+              else if (pos < d.nvalid) lm = fmaxf(lm, __ldg(wrow + d.e0 + pos));
             }
           }
         }
       }
-      c = __reduce_add_sync(0xFFFFFFFFu, c);
-      if (lane == 0) atomicAdd(&st.warm_cnt, c);
+      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, Top4::key_of(lm));
+      if (lane == 0) st.est3[swarp] = wmax;
+      if (stt == 0) {
+        st.spec_cnt[0] = 0u;
+        st.spec_cnt[1] = 0u;
+      }
       Sel::sync();
-      if (st.warm_cnt >= uint32_t(k)) mk = mc;
+      // the three smallest warp maxima
+      uint32_t s8 = 0xFFFFFFFFu, s7 = 0xFFFFFFFFu, s6 = 0xFFFFFFFFu;
+#pragma unroll
+      for (int q = 0; q < kNS; ++q) {
+        const uint32_t v = st.est3[q];
+        const uint32_t n8 = min(s8, v), n7 = min(s7, max(s8, v)), n6 = min(s6, max(s7, v));
+        s8 = n8;
+        s7 = n7;
+        s6 = n6;
+      }
+      if (s8 > 1u) {  // (every warp saw a value)
+        const float f8 = key_to_float(s8 - 1u), f7 = key_to_float(s7 - 1u),
+                    f6 = key_to_float(s6 - 1u);  // key >= s  <=>  value > key_to_float(s - 1)
+        uint32_t ca = 0u, cb = 0u;               // counts: s8 | s7 << 16, and s6
+        for (int q = 0; q < wu; ++q) {
+          const float* src;
+          StageDesc d;
+          uint32_t copied;
+          stage_of(q, src, d, copied);
+          if (copied == uint32_t(kUnit)) {
+#pragma unroll 4
+            for (int u = 0; u < kF4; ++u) {
+              const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
+              const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                ca += (vv[c] > f8 ? 1u : 0u) + (vv[c] > f7 ? 0x10000u : 0u);
+                cb += vv[c] > f6 ? 1u : 0u;
+              }
+            }
+          } else {
+            for (int u = 0; u < kF4; ++u) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint32_t pos = uint32_t(4 * (stt + kNST * u) + c);
+                float v = -__int_as_float(0x7F800000);
+                if (pos < copied) v = src[pos];
+                else if (pos < d.nvalid) v = __ldg(wrow + d.e0 + pos);
+                ca += (v > f8 ? 1u : 0u) + (v > f7 ? 0x10000u : 0u);
+                cb += v > f6 ? 1u : 0u;
+              }
+            }
+          }
+        }
+        ca = __reduce_add_sync(0xFFFFFFFFu, ca);
+        cb = __reduce_add_sync(0xFFFFFFFFu, cb);
+        if (lane == 0) {
+          atomicAdd(&st.spec_cnt[0], ca);
+          atomicAdd(&st.spec_cnt[1], cb);
+        }
+        Sel::sync();
+        const uint32_t n8 = st.spec_cnt[0] & 0xFFFFu, n7 = st.spec_cnt[0] >> 16,
+                       n6 = st.spec_cnt[1];
+        uint32_t sk = 0u, nk = 0u;
+        if (n6 >= need) {
+          sk = s6;
+          nk = n6;
+        } else if (n7 >= need) {
+          sk = s7;
+          nk = n7;
+        } else if (n8 >= need) {
+          sk = s8;
+          nk = n8;
+        }
+        if (sk != 0u) {
+          // a candidate the sample alone shows k elements above is proven
+          if (nk >= uint32_t(k)) mk = sk;
+          else spec = (uint64_t(sk) << 32) - 1ull;
+          decided = true;
+        }
+      }
+    }
+  }
+  if (!decided) {
+    if (m_warm > 64) {
+      // one unit, all 32 keys of every lane
+      const float* src;
+      StageDesc d;
+      uint32_t copied;
+      stage_of(0, src, d, copied);
+      float x[kEPT];
+      const uint32_t valid = load_share(x, src, wrow, d.e0, d.nvalid, copied, stt);
+      const uint32_t est = warp_key_bound(x, valid, m_warm);
+      if (lane == 0) st.est[swarp] = est;
+      Sel::sync();
+      mk = 0xFFFFFFFFu;
+#pragma unroll
+      for (int q = 0; q < kNS; ++q) mk = min(mk, st.est[q]);
+    } else {
+      // Lane lists of the first unit give two bounds per warp: a safe one
+      // (m elements of the unit) and a candidate for all wu units (about
+      // 1.25 m / wu elements of the unit).  The candidate is taken if a count
+      // finds k elements at or above it: the lane lists' count in the first
+      // unit (a lower bound) plus a strict float compare over the other units
+      // (it never counts NaN, and misses only -0.0 against a +0.0 bound).
+      Top4 top;
+      {
+        const float* src;
+        StageDesc d;
+        uint32_t copied;
+        stage_of(0, src, d, copied);
+        if (copied == uint32_t(kUnit)) {
+#pragma unroll 2
+          for (int u = 0; u < kF4; ++u) top.add4(reinterpret_cast<const float4*>(src)[stt + kNST * u]);
+        } else {
+          for (int u = 0; u < kF4; ++u) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t pos = uint32_t(4 * (stt + kNST * u) + c);
+              if (pos < copied) top.add(Top4::key_of(src[pos]));
+              else if (pos < d.nvalid) top.add(Top4::key_of(__ldg(wrow + d.e0 + pos)));
+            }
+          }
+        }
+      }
+      const int m_c = wu > 1 ? (5 * m_warm + 4 * wu - 1) / (4 * wu) : m_warm;
+      uint32_t es, ec;
+      top.bound2(m_warm, m_c, es, ec);
+      if (lane == 0) {
+        st.est[swarp] = es;
+        st.est2[swarp] = ec;
+      }
+      Sel::sync();
+      uint32_t ms = 0xFFFFFFFFu, mc = 0xFFFFFFFFu;
+#pragma unroll
+      for (int q = 0; q < kNS; ++q) {
+        ms = min(ms, st.est[q]);
+        mc = min(mc, st.est2[q]);
+      }
+      mk = ms;
+      if (wu > 1 && mc > ms) {
+        uint32_t c = top.count_ge(mc);
+        const float flo = key_to_float(mc - 1u);  // key >= mc  <=>  value > flo
+        for (int q = 1; q < wu; ++q) {
+          const float* src;
+          StageDesc d;
+          uint32_t copied;
+          stage_of(q, src, d, copied);
+          if (copied == uint32_t(kUnit)) {
+#pragma unroll 4
+            for (int u = 0; u < kF4; ++u) {
+              const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
+              c += (v.x > flo ? 1u : 0u) + (v.y > flo ? 1u : 0u) + (v.z > flo ? 1u : 0u) +
+                   (v.w > flo ? 1u : 0u);
+            }
+          } else {
+            for (int u = 0; u < kF4; ++u) {
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t pos = uint32_t(4 * (stt + kNST * u) + cc);
+                float v = -__int_as_float(0x7F800000);
+                if (pos < copied) v = src[pos];
+                else if (pos < d.nvalid) v = __ldg(wrow + d.e0 + pos);
+                c += v > flo ? 1u : 0u;
+              }
+            }
+          }
+        }
+        c = __reduce_add_sync(0xFFFFFFFFu, c);
+        if (lane == 0) atomicAdd(&st.warm_cnt, c);
+        Sel::sync();
+        if (st.warm_cnt >= uint32_t(k)) mk = mc;
+      }
     }
   }
   if (stt == 0) {
@@ -836,6 +973,14 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
       // selector loop reads their thresholds back)
       if (pw.contributors > 1) atomicMax(&row_theta[pw.r], (unsigned long long)th0);
       atomicMax(&st.theta[w & 1], (unsigned long long)th0);
+    }
+    // A speculative threshold stays with this CTA (the row's other pieces
+    // may adopt it as theirs, never as a proven bound); the row's end checks
+    // it against the row's k-th word.
+    if (spec > th0) {
+      if (pw.contributors > 1) atomicMax(&row_spec[pw.r], (unsigned long long)spec);
+      atomicMax(&st.theta[w & 1], (unsigned long long)spec);
+      st.spec[w & 1] = spec;
     }
     __threadfence_block();
     *reinterpret_cast<volatile int*>(&st.warm_pub) = w + 1;
@@ -880,6 +1025,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       st.tail[q] = 0;
       st.fdone[q] = 0;
       st.theta[q] = 0ull;
+      st.spec[q] = 0ull;
     }
     st.sel_pieces = 0;
     st.pieces_pub = 0;
@@ -898,6 +1044,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   // ---------------- producer: the plan, a2 visiting orders, a3 copies ----------------
   if (warp == kProducerWarp) {
     const bool identity = (p.flags & TOPK_FLAG_IDENTITY_ORDER) != 0;
+    // scores are read once: their lines go first when L2 needs room
+    const uint64_t l2pol = l2_policy_evict_first();
     bool gave_up = false;
     uint32_t g = 0;  // stages issued (lane 0)
     int stage = 0;
@@ -991,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             fence_proxy_async_smem();
             if (bytes) {
               mbar_arrive_expect_tx(&full[stage], bytes);
-              bulk_load(ring + stage * kUnit, row + e0, bytes, &full[stage]);
+              bulk_load_hint(ring + stage * kUnit, row + e0, bytes, &full[stage], l2pol);
             } else {
               mbar_arrive(&full[stage]);
             }
@@ -1193,21 +1341,26 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   int tray_n = 0;       // words in the tray
   int kept_n = 0;       // real words in the kept list
   int pruned = 0;       // tray words left by the last prune
-  uint64_t theta = 0ull;
+  uint64_t theta = 0ull;         // the piece's threshold word (proven or speculative)
+  uint64_t theta_proven = 0ull;  // the largest proven word this piece has published
   uint32_t head = 0, head_other = 0;  // inbox heads: this piece's parity, the other one
   int par = 0;
   int warm_next = 0;  // next piece whose starting threshold is to be set
 
   // Publish a threshold to the filters (and to the row's other CTAs).
+  // Every word passed here is proven: at least k words of the row are at or
+  // above it.  (The threshold word the filters use may also hold a
+  // speculative start, which is never shared as a proven bound.)
   auto raise_theta = [&](uint64_t nth, const Piece& pc) {
-    if (nth <= theta) return;
-    theta = nth;
-    if (stt == 0) {
+    if (nth > theta_proven) {
+      theta_proven = nth;
       // shared with the row's other CTAs without waiting for the reply (the
       // selector loop reads their thresholds back)
-      if (pc.contributors > 1) atomicMax(&p.row_theta[pc.r], (unsigned long long)nth);
-      atomicMax(&st.theta[par], (unsigned long long)nth);
+      if (stt == 0 && pc.contributors > 1) atomicMax(&p.row_theta[pc.r], (unsigned long long)nth);
     }
+    if (nth <= theta) return;
+    theta = nth;
+    if (stt == 0) atomicMax(&st.theta[par], (unsigned long long)nth);
   };
 
   // a6: the tray.  A byte-wise histogram select over kept + tray finds a word
@@ -1360,6 +1513,54 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     if (stt == 0) *reinterpret_cast<volatile uint32_t*>(&st.head[par]) = head;
   };
 
+  // A row whose speculative start missed (fewer than k of its words lie above
+  // the largest speculative threshold its pieces started from) is selected
+  // again, exactly, by this team alone from global memory: every word of the
+  // row at or above `lb` goes through the tray into a fresh kept list.  `lb`
+  // is a word the row's k-th word is known to reach (a word of the row's
+  // merged or kept list), or 0.
+  auto rescan = [&](const Piece& pc, uint64_t lb) {
+    const float* rrow = p.scores + int64_t(pc.r) * p.row_stride;
+    for (int q = stt; q < kp; q += kNST) kept[q] = 0ull;
+    kept_n = 0;
+    tray_n = 0;
+    pruned = 0;
+    theta = lb ? lb - 1ull : 0ull;
+    if (stt == 0) atomicOr(p.status, TOPK_STATUS_RESCAN);
+    Sel::sync();
+    constexpr int R = kRescanChunk / kNST;
+    static_assert(kRescanChunk % kNST == 0 && kTray >= 2 * kRescanChunk - 1024,
+                  "a rescan step fits the tray after a sort");
+    for (uint32_t b0 = 0; b0 < pc.L; b0 += uint32_t(kRescanChunk)) {
+      if (tray_n + kRescanChunk > kTray) process_tray(true, false, pc);
+      if (stt == 0) st.cnt2 = 0;
+      Sel::sync();
+      uint32_t bits[R];
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        const uint32_t e = b0 + uint32_t(u * kNST + stt);
+        bits[u] = e < pc.L ? __float_as_uint(rrow[e]) : 0x7FFFFFFFu;  // (past the end: a NaN)
+      }
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        const uint32_t e = b0 + uint32_t(u * kNST + stt);
+        const uint64_t w = (uint64_t(order_key(bits[u])) << 32) | uint64_t(~e);
+        const bool keep = (bits[u] & 0x7FFFFFFFu) <= 0x7F800000u && w > theta;  // NaN never
+        const uint32_t mask = __ballot_sync(0xFFFFFFFFu, keep);
+        if (mask) {
+          int at = 0;
+          if (lane == 0) at = atomicAdd(&st.cnt2, __popc(mask));
+          at = __shfl_sync(0xFFFFFFFFu, at, 0);
+          if (keep) tray[tray_n + at + __popc(mask & lt_mask)] = w;
+        }
+      }
+      Sel::sync();
+      tray_n += st.cnt2;
+      Sel::sync();
+    }
+    if (tray_n > 0) process_tray(true, true, pc);
+  };
+
   for (int j = 0;; ++j) {
     // the producer publishes piece j's descriptor before its first stage
     if (stt == 0) {
@@ -1415,8 +1616,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
                 pn.contributors > 1
                     ? *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[pn.r])
                     : 0ull;
-            if (rt != 0ull) {
-              atomicMax(&st.theta[warm_next & 1], rt);
+            // a speculative start of the row's other pieces is adopted as
+            // this piece's own (the row's end checks the largest of them)
+            const unsigned long long rs =
+                pn.contributors > 1
+                    ? *reinterpret_cast<volatile unsigned long long*>(&p.row_spec[pn.r])
+                    : 0ull;
+            if (rt != 0ull || rs != 0ull) {
+              if (rt != 0ull) atomicMax(&st.theta[warm_next & 1], rt);
+              if (rs > rt) {
+                atomicMax(&st.theta[warm_next & 1], rs);
+                st.spec[warm_next & 1] = rs;
+              }
               __threadfence_block();
               *reinterpret_cast<volatile int*>(&st.warm_pub) = warm_next + 1;
               warm = 2;
@@ -1479,8 +1690,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (sth > theta) theta = sth;
       Sel::sync();
       if (warm) {
-        if (warm == 1 && !warm_start_piece(p.scores, p.row_stride, p.row_theta, st, warm_next, ring,
-                                           desc, full, nstage, k, stt))
+        if (warm == 1 && !warm_start_piece(p.scores, p.row_stride, p.row_theta, p.row_spec, st,
+                                           warm_next, ring, desc, full, nstage, k, stt))
           timed_out = true;
         ++warm_next;
         continue;
@@ -1494,6 +1705,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     // end of the piece: final sort, then the row's output (directly, or
     // through the split-row ticket)
     if (tray_n > 0) process_tray(true, true, pc);
+    // A row whose pieces started from speculative thresholds is selected
+    // again if its k-th word does not lie above the largest of them.
+    bool redo = false;
+    uint64_t redo_lb = 0ull;
     if (stt == 0) {
       atomicAdd(&p.sorts[pc.r], nsorts);
       atomicAdd(&p.survivors[pc.r], nsorted);
@@ -1501,7 +1716,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     nsorts = 0;
     nsorted = 0;
     if (pc.contributors == 1) {
-      write_row(p, pc.r, kept, stt, kNST);
+      const uint64_t spec_p = st.spec[par];
+      if (spec_p != 0ull && kept[k - 1] <= spec_p) {
+        redo = true;
+        redo_lb = kept[k - 1];
+      } else {
+        write_row(p, pc.r, kept, stt, kNST);
+      }
     } else {
       // a7: publish the local list, take a ticket; the last ticket merges.
       uint64_t* mine = p.partials + int64_t(pc.slot) * kp;
@@ -1562,16 +1783,40 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             }
           }
         }
-        write_row(p, pc.r, slots, stt, kNST);
+        // the row's k-th word must lie above every speculative threshold its
+        // pieces started from, else the row is selected again
+        const uint64_t rs = *reinterpret_cast<volatile unsigned long long*>(&p.row_spec[pc.r]);
+        const uint64_t wk = slots[k - 1];
+        Sel::sync();
+        if (rs != 0ull && wk <= rs) {
+          redo = true;
+          redo_lb = wk;
+        } else {
+          write_row(p, pc.r, slots, stt, kNST);
+        }
         Sel::sync();
         uint64_t* ib = par ? inbox1 : inbox0;
         for (int q = stt; q < kInbox; q += kNST) ib[q] = 0ull;  // empty slots again
         __threadfence_block();
         if (stt == 0) {
           p.row_theta[pc.r] = 0ull;
+          p.row_spec[pc.r] = 0ull;
           atomicExch(&p.tickets[pc.r], 0u);
         }
       }
+    }
+    if (redo) {
+      // (as a lone piece: the row's shared words are already reset)
+      Piece lone = pc;
+      lone.contributors = 1;
+      rescan(lone, redo_lb);
+      if (stt == 0) {
+        atomicAdd(&p.sorts[pc.r], nsorts);
+        atomicAdd(&p.survivors[pc.r], nsorted);
+      }
+      nsorts = 0;
+      nsorted = 0;
+      write_row(p, pc.r, kept, stt, kNST);
     }
     // a clean tray and threshold, then hand this parity back to the filters
     Sel::sync();
@@ -1580,9 +1825,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     kept_n = 0;
     pruned = 0;
     theta = 0ull;
+    theta_proven = 0ull;
     Sel::sync();
     if (stt == 0) {
       *reinterpret_cast<volatile unsigned long long*>(&st.theta[par]) = 0ull;
+      st.spec[par] = 0ull;
       __threadfence_block();
       *reinterpret_cast<volatile int*>(&st.sel_pieces) = j + 1;
     }
@@ -1769,6 +2016,7 @@ int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_str
   p.sorts = reinterpret_cast<uint32_t*>(w + wl.sorts);
   p.admitted = reinterpret_cast<uint32_t*>(w + wl.admitted);
   p.row_theta = reinterpret_cast<unsigned long long*>(w + wl.theta);
+  p.row_spec = reinterpret_cast<unsigned long long*>(w + wl.spec);
   p.partials = reinterpret_cast<uint64_t*>(w + wl.partials);
   p.seed_lo = uint32_t(seed);
   p.seed_hi = uint32_t(seed >> 32);
