@@ -99,13 +99,17 @@ constexpr int kWarmUnits = 4;                // units a warm start reads (k <= 5
 // (k <= 512 runs a five-stage ring: the producer can land all warm-start
 // units of a piece while the filters hold its first one)
 static_assert(kWarmUnits <= 5, "warm-start units fit in the ring");
-// Speculative start: a piece of at least kSpecMinUnits units may start from a
-// threshold its warm-start units only make likely (about 3.6 k words of the
-// row above it).  It is taken when those units hold at least
-// 2.5 k * sample / row length elements at or above it, at most kSpecMaxNeed.
-constexpr int kSpecMinUnits = 16;
+// Speculative start: a piece with kWarmUnits warm-start units may start from a
+// threshold those units only make likely (about 3.6 k words of the row above
+// it).  It is taken when they hold at least 2.5 k * sample / row length
+// elements at or above it, at most kSpecMaxNeed (so: long rows).
 constexpr uint32_t kSpecMaxNeed = 128;
 constexpr int kRescanChunk = 2048;           // row elements a rescan step reads
+// Pre-final: when a piece of at least kPreFinalMin units is within kPreFinal
+// stages of its end, the selectors sort what they hold, so that its end only
+// merges the words of the last stages.
+constexpr int kPreFinal = 8;
+constexpr int kPreFinalMin = 16;
 constexpr int kMaxSplit = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls before a wait gives up
 
@@ -328,10 +332,13 @@ struct CtaState {
   uint32_t est2[kNS];              // warm start: per selector warp candidate bound
   uint32_t warm_cnt;               // warm start: elements reaching the candidate
   uint32_t est3[kNS];              // warm start: per selector warp largest key
-  uint32_t spec_cnt[2];            // warm start: sample counts of the speculative bounds
+  uint32_t spec_cnt[3];            // warm start: sample counts of the speculative bounds
+  uint32_t est4[kNS];              // warm start: per selector warp smallest unit maximum
   unsigned long long spec[2];      // speculative threshold word of the piece using inbox p
   int warm_pub;                    // pieces whose starting threshold is set
   int first_issued;                // pieces whose first stage the producer has issued
+  uint32_t fprog;                  // stages filter warp 0 has released
+  int sel_pre;                     // selector step: pre-final due
   unsigned long long theta[2];     // threshold word of the piece using inbox p
   Piece table[kTable];             // piece descriptors, by sequence number
 };
@@ -766,7 +773,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
   // never counts NaN, and misses only -0.0 against a +0.0 bound).  Only when
   // no candidate is supported do the lane lists below run.
   const int nu = pw.u_end - pw.u_begin;
-  if (m_warm <= 64 && wu == kWarmUnits && nu >= kSpecMinUnits) {
+  if (m_warm <= 64 && wu == kWarmUnits && nu >= kWarmUnits) {
     const uint64_t sample = uint64_t(wu) * uint64_t(kUnit);
     const uint64_t need64 = (5ull * uint64_t(k) * sample + 2ull * pw.L - 1ull) / (2ull * pw.L);
     if (need64 <= kSpecMaxNeed) {
@@ -799,6 +806,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
       if (stt == 0) {
         st.spec_cnt[0] = 0u;
         st.spec_cnt[1] = 0u;
+        st.spec_cnt[2] = 0u;
       }
       Sel::sync();
       // the three smallest warp maxima
@@ -815,16 +823,19 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
         const float f8 = key_to_float(s8 - 1u), f7 = key_to_float(s7 - 1u),
                     f6 = key_to_float(s6 - 1u);  // key >= s  <=>  value > key_to_float(s - 1)
         uint32_t ca = 0u, cb = 0u;               // counts: s8 | s7 << 16, and s6
+        uint32_t umin = 0xFFFFFFFFu;             // smallest of this warp's unit maxima
         for (int q = 0; q < wu; ++q) {
           const float* src;
           StageDesc d;
           uint32_t copied;
           stage_of(q, src, d, copied);
+          float um = -__int_as_float(0x7F800000);
           if (copied == uint32_t(kUnit)) {
 #pragma unroll 4
             for (int u = 0; u < kF4; ++u) {
               const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
               const float vv[4] = {v.x, v.y, v.z, v.w};
+              um = fmaxf(um, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 ca += (vv[c] > f8 ? 1u : 0u) + (vv[c] > f7 ? 0x10000u : 0u);
@@ -839,17 +850,20 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
                 float v = -__int_as_float(0x7F800000);
                 if (pos < copied) v = src[pos];
                 else if (pos < d.nvalid) v = __ldg(wrow + d.e0 + pos);
+                um = fmaxf(um, v);
                 ca += (v > f8 ? 1u : 0u) + (v > f7 ? 0x10000u : 0u);
                 cb += v > f6 ? 1u : 0u;
               }
             }
           }
+          umin = min(umin, __reduce_max_sync(0xFFFFFFFFu, Top4::key_of(um)));
         }
         ca = __reduce_add_sync(0xFFFFFFFFu, ca);
         cb = __reduce_add_sync(0xFFFFFFFFu, cb);
         if (lane == 0) {
           atomicAdd(&st.spec_cnt[0], ca);
           atomicAdd(&st.spec_cnt[1], cb);
+          st.est4[swarp] = umin;
         }
         Sel::sync();
         const uint32_t n8 = st.spec_cnt[0] & 0xFFFFu, n7 = st.spec_cnt[0] >> 16,
@@ -864,6 +878,49 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
         } else if (n8 >= need) {
           sk = s8;
           nk = n8;
+        }
+        if (sk == 0u) {
+          // Second round: the smallest of the 32 (warp, unit) maxima of the
+          // sample, a lower candidate, counted the same way.
+          uint32_t s2 = 0xFFFFFFFFu;
+#pragma unroll
+          for (int q = 0; q < kNS; ++q) s2 = min(s2, st.est4[q]);
+          if (s2 > 1u && s2 < s8) {
+            const float f2 = key_to_float(s2 - 1u);
+            uint32_t c2 = 0u;
+            for (int q = 0; q < wu; ++q) {
+              const float* src;
+              StageDesc d;
+              uint32_t copied;
+              stage_of(q, src, d, copied);
+              if (copied == uint32_t(kUnit)) {
+#pragma unroll 4
+                for (int u = 0; u < kF4; ++u) {
+                  const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
+                  c2 += (v.x > f2 ? 1u : 0u) + (v.y > f2 ? 1u : 0u) + (v.z > f2 ? 1u : 0u) +
+                        (v.w > f2 ? 1u : 0u);
+                }
+              } else {
+                for (int u = 0; u < kF4; ++u) {
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) {
+                    const uint32_t pos = uint32_t(4 * (stt + kNST * u) + c);
+                    float v = -__int_as_float(0x7F800000);
+                    if (pos < copied) v = src[pos];
+                    else if (pos < d.nvalid) v = __ldg(wrow + d.e0 + pos);
+                    c2 += v > f2 ? 1u : 0u;
+                  }
+                }
+              }
+            }
+            c2 = __reduce_add_sync(0xFFFFFFFFu, c2);
+            if (lane == 0) atomicAdd(&st.spec_cnt[2], c2);
+            Sel::sync();
+            if (st.spec_cnt[2] >= need) {
+              sk = s2;
+              nk = st.spec_cnt[2];
+            }
+          }
         }
         if (sk != 0u) {
           // a candidate the sample alone shows k elements above is proven
@@ -1032,6 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     st.npieces = -1;
     st.warm_pub = 0;
     st.first_issued = 0;
+    st.fprog = 0u;
     st.flags = 0;
     for (int i = 0; i < nstage; ++i) {
       mbar_init(&full[i], 1);
@@ -1180,6 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     uint64_t th = 0ull;
     float thf = threshold_float(th);
     uint32_t admitted = 0;
+    uint32_t released = 0;  // stages released (kept by warp 0 for the selectors)
     bool saw_nan = false, timed_out = false;
     int stage = 0;
     uint32_t phase = 0;
@@ -1307,7 +1366,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (lane == 0) {
+        mbar_arrive(&empty[stage]);
+        if (warp == 0) *reinterpret_cast<volatile uint32_t*>(&st.fprog) = ++released;
+      }
       if (d.tag & kLast) {
         __syncwarp();
         admitted = __reduce_add_sync(0xFFFFFFFFu, admitted);
@@ -1595,6 +1657,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       head_other = h;
     }
     const int fd_target = kNF * (j / 2 + 1);
+    const int pc_nu = pc.u_end - pc.u_begin;
+    const uint32_t pre_at = pc.g_first + uint32_t(pc_nu) - uint32_t(kPreFinal);
+    bool pre_done = pc_nu < kPreFinalMin;
 
     for (;;) {
       // One lane polls until there is a batch to take or the piece is done;
@@ -1602,7 +1667,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       // is read before the tail, so a full count means the tail is final.
       if (stt == 0) {
         uint32_t it = timed_out ? kWaitLimit : 0u;
-        int n = 0, done = 0, warm = 0;
+        int n = 0, done = 0, warm = 0, pre = 0;
         for (;;) {
           // First: a piece (this one or the next) still waiting for its
           // starting threshold.  A split row whose other CTAs have already
@@ -1670,6 +1735,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
                 *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[pc.r]);
             if (gt > theta) atomicMax(&st.theta[par], gt);
           }
+          // near the piece's end: take everything there is and sort it
+          if (!pre_done && !done &&
+              int32_t(*reinterpret_cast<volatile uint32_t*>(&st.fprog) - pre_at) >= 0) {
+            pre = 1;
+            n = int(min(avail, uint32_t(kTray - tray_n)));
+            if (n > kTakeMax) n = kTakeMax;
+            break;
+          }
           if (n > 0 || done) break;
           if (++it > kWaitLimit) {
             timed_out = true;
@@ -1681,11 +1754,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         st.sel_n = n;
         st.sel_done = done;
         st.flags = warm;
+        st.sel_pre = pre;
       }
       Sel::sync();
       const int n = st.sel_n;
       const bool done = st.sel_done != 0;
       const int warm = st.flags;
+      const bool pre = st.sel_pre != 0;
       const uint64_t sth = *reinterpret_cast<volatile unsigned long long*>(&st.theta[par]);
       if (sth > theta) theta = sth;
       Sel::sync();
@@ -1696,6 +1771,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         ++warm_next;
         continue;
       }
+      if (pre) {
+        pre_done = true;
+        if (n > 0) take(n);
+        if (tray_n > 0) process_tray(true, true, pc);
+        continue;
+      }
       if (done) break;
       take(n);
       if (tray_n >= kTrayMark) process_tray(true, false, pc);
@@ -1704,7 +1785,22 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
 
     // end of the piece: final sort, then the row's output (directly, or
     // through the split-row ticket)
-    if (tray_n > 0) process_tray(true, true, pc);
+    if (tray_n > 0) {
+      if (kept_n > 0 && tray_n <= kNST && kp >= kNST) {
+        // Only the last stages' words are left (the kept list holds the best
+        // kp of everything before): sort them and merge, no select needed.
+        for (int t = tray_n + stt; t < kNST; t += kNST) tray[t] = 0ull;
+        Sel::sync();
+        team_sort_desc<Sel>(tray, kNST, 2, stt);
+        merge_into_kept<Sel>(kept, tray, kNST, kp, stt);
+        ++nsorts;
+        nsorted += uint32_t(tray_n);
+        kept_n = min(kp, kept_n + tray_n);
+        tray_n = 0;
+      } else {
+        process_tray(true, true, pc);
+      }
+    }
     // A row whose pieces started from speculative thresholds is selected
     // again if its k-th word does not lie above the largest of them.
     bool redo = false;
