@@ -335,6 +335,7 @@ struct CtaState {
   uint32_t spec_cnt[3];            // warm start: sample counts of the speculative bounds
   uint32_t est4[kNS];              // warm start: per selector warp smallest unit maximum
   unsigned long long spec[2];      // speculative threshold word of the piece using inbox p
+  const uint64_t* gsrc[16];        // leader merge: the partial lists of one gather step
   int warm_pub;                    // pieces whose starting threshold is set
   int first_issued;                // pieces whose first stage the producer has issued
   uint32_t fprog;                  // stages filter warp 0 has released
@@ -1832,19 +1833,23 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       Sel::sync();
       if (st.leader) {
         __threadfence();
+        // (read now, used after the merge: the row's pieces all published
+        // their speculative words before their tickets)
+        const uint64_t rs = *reinterpret_cast<volatile unsigned long long*>(&p.row_spec[pc.r]);
         // Gather lists into this piece's (drained) inbox + the tray and merge
         // them as a tree of parallel pairwise merges; the running result
         // stays in slot 0.
         uint64_t* slots = par == 0 ? inbox0 : tray;  // kInbox + kTray contiguous words
         const int cap = (kInbox + kTray) / kp;
+        const int lkp = __ffs(kp) - 1;
         for (int q = stt; q < kp; q += kNST) slots[q] = kept[q];
-        int next_other = 0;  // next contributor to gather (never this CTA)
+        int gathered = 0;  // other contributors gathered so far (never this CTA)
         int remaining = pc.contributors - 1;
         while (remaining > 0) {
-          const int takeq = min(remaining, cap - 1);
-          int o = next_other;
-          for (int q = 1; q <= takeq; ++q, ++o) {
-            if (o == pc.self) ++o;
+          const int takeq = min(remaining, min(cap - 1, 16));
+          if (stt < takeq) {
+            const int i = gathered + stt;
+            const int o = i + (i >= pc.self ? 1 : 0);  // contributor index
             int64_t slot;
             if (p.plan == kPlanItems) {
               slot = int64_t(pc.r) * p.split + o;
@@ -1853,10 +1858,25 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               const int64_t go = pc.first_cta + o;
               slot = 2 * go + (flat_lo(go, M, G) / p.u_full == pc.r ? 0 : 1);
             }
-            const uint64_t* other = p.partials + slot * kp;
-            for (int q2 = stt; q2 < kp; q2 += kNST) slots[q * kp + q2] = __ldcg(other + q2);
+            st.gsrc[stt] = p.partials + slot * kp;
           }
-          next_other = o;
+          Sel::sync();
+          // every word of the step with eight loads in flight per thread
+          const int total = takeq * kp;
+          for (int b = stt; b < total; b += 8 * kNST) {
+            uint64_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int t = b + u * kNST;
+              v[u] = t < total ? __ldcg(st.gsrc[t >> lkp] + (t & (kp - 1))) : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int t = b + u * kNST;
+              if (t < total) slots[kp + t] = v[u];
+            }
+          }
+          gathered += takeq;
           remaining -= takeq;
           Sel::sync();
           const int nl = takeq + 1;
@@ -1881,7 +1901,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         }
         // the row's k-th word must lie above every speculative threshold its
         // pieces started from, else the row is selected again
-        const uint64_t rs = *reinterpret_cast<volatile unsigned long long*>(&p.row_spec[pc.r]);
         const uint64_t wk = slots[k - 1];
         Sel::sync();
         if (rs != 0ull && wk <= rs) {
