@@ -2,13 +2,16 @@
 
 A ctypes loader for ``topk_oracle.cpp``, the plain single-threaded C++
 statement of the selection (sort every valid row prefix by value descending,
-ties to the smaller index; pad short rows with (-inf, -1)).  Only the tests,
+ties to the smaller index; pad short rows with (-inf, -1)) and of the
+layer-20 block pool (blocks of consecutive positions scored by their largest
+value; the newest blocks pinned, then the best others; ascending indices).  Only the tests,
 ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may use it;
 the library under ``sparse_attention_indexer_row_gb300`` never does.
 
-Parity status: pinned.  ``tests/test_oracle.py`` checks it against brute-force
-enumeration, repeated argmax, closed forms, numpy's lexsort and invariants, and
-compiles mutants of it to show that each pin bites.
+Parity status: pinned, both functions.  ``tests/test_oracle.py`` checks them
+against brute-force enumeration, repeated argmax, closed forms, numpy's
+lexsort and invariants, and compiles mutants of them to show that each pin
+bites.
 """
 
 from __future__ import annotations
@@ -53,6 +56,12 @@ class Oracle:
             ctypes.c_int32,
         ]
         lib.oracle_hardware_threads.restype = ctypes.c_int32
+        lib.oracle_block_pool.restype = ctypes.c_int
+        lib.oracle_block_pool.argtypes = [
+            ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_void_p, ctypes.c_int32,
+        ]
         self._lib = lib
 
     def hardware_threads(self) -> int:
@@ -82,6 +91,27 @@ class Oracle:
         return vals, idx, int(st)
 
 
+    def block_pool(self, scores: np.ndarray, block: int, pool: int, pinned: int,
+                   lengths: np.ndarray | None = None, n: int | None = None, nthreads: int = 1):
+        """Block pool of every row (see oracle_block_pool in topk_oracle.cpp).
+
+        Returns (blocks int32[rows, pool], status int).
+        """
+        scores = np.ascontiguousarray(scores, dtype=np.float32)
+        assert scores.ndim == 2
+        rows, stride = scores.shape
+        n = stride if n is None else int(n)
+        out = np.empty((rows, pool), dtype=np.int32)
+        lp = None
+        if lengths is not None:
+            lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+            assert lengths.shape == (rows,)
+            lp = lengths.ctypes.data
+        st = self._lib.oracle_block_pool(scores.ctypes.data, rows, n, stride, lp, block, pool,
+                                         pinned, out.ctypes.data, nthreads)
+        return out, int(st)
+
+
 _DEFAULT: Oracle | None = None
 
 
@@ -100,3 +130,7 @@ def load(mutant: int = 0) -> Oracle:
 
 def topk(scores, k, lengths=None, n=None, nthreads=1):
     return load().topk(scores, k, lengths=lengths, n=n, nthreads=nthreads)
+
+
+def block_pool(scores, block, pool, pinned, lengths=None, n=None, nthreads=1):
+    return load().block_pool(scores, block, pool, pinned, lengths=lengths, n=n, nthreads=nthreads)

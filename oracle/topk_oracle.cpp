@@ -116,6 +116,68 @@ int select_row(const float* row, int64_t len, int32_t k, float* vals,
   return 0;
 }
 
+// a is a larger value than b in the same total order (+0.0 above -0.0).
+bool value_greater(float a, float b) {
+  if (a > b) return true;
+  if (a < b) return false;
+  return !std::signbit(a) && std::signbit(b);
+}
+
+// The block pool of one row.  Returns 0, or 5 when a NaN sits inside the
+// valid prefix (the row's pool is then all -1).
+int pool_row(const float* row, int64_t len, int32_t block, int32_t pool,
+             int32_t pinned, int32_t* out) {
+  for (int32_t j = 0; j < pool; ++j) out[j] = -1;
+  for (int64_t i = 0; i < len; ++i)
+    if (std::isnan(row[i])) return 5;
+#if ORACLE_MUTANT == 13
+  const int64_t nb = len / block;  // mistake: the short last block is dropped
+#else
+  const int64_t nb = (len + block - 1) / block;
+#endif
+  const int64_t pe = std::min<int64_t>(pinned, nb);
+#if ORACLE_MUTANT == 14
+  const int64_t ncand = nb;  // mistake: pinned blocks also compete
+#else
+  const int64_t ncand = nb - pe;
+#endif
+  // each candidate block's score: the largest value inside it
+  std::vector<float> bmax(static_cast<size_t>(ncand));
+  for (int64_t b = 0; b < ncand; ++b) {
+    const int64_t lo = b * block, hi = std::min<int64_t>(len, lo + block);
+    float m = row[lo];
+#if ORACLE_MUTANT != 10  // mistake 10: the block's first score stands for it
+    for (int64_t i = lo + 1; i < hi; ++i)
+      if (value_greater(row[i], m)) m = row[i];
+#else
+    (void)hi;
+#endif
+    bmax[static_cast<size_t>(b)] = m;
+  }
+  std::vector<int64_t> order(static_cast<size_t>(ncand));
+  for (int64_t b = 0; b < ncand; ++b) order[static_cast<size_t>(b)] = b;
+  std::sort(order.begin(), order.end(), [&bmax](int64_t a, int64_t b) {
+#if ORACLE_MUTANT == 12
+    return ranks_before(bmax[a], -a, bmax[b], -b);  // mistake: ties to the larger block
+#else
+    return ranks_before(bmax[a], a, bmax[b], b);
+#endif
+  });
+  std::vector<int64_t> kept;
+  const int64_t take = std::min<int64_t>(pool - pe, ncand);
+  for (int64_t j = 0; j < take; ++j) kept.push_back(order[static_cast<size_t>(j)]);
+#if ORACLE_MUTANT == 11
+  for (int64_t b = 0; b < pe; ++b) kept.push_back(b);  // mistake: oldest blocks pinned
+#else
+  for (int64_t b = nb - pe; b < nb; ++b) kept.push_back(b);
+#endif
+  std::sort(kept.begin(), kept.end());
+  kept.erase(std::unique(kept.begin(), kept.end()), kept.end());
+  for (size_t j = 0; j < kept.size() && j < static_cast<size_t>(pool); ++j)
+    out[j] = static_cast<int32_t>(kept[j]);
+  return 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -165,6 +227,59 @@ int oracle_topk(const float* scores, int32_t rows, int64_t n,
     std::vector<std::thread> pool;
     for (int32_t t = 0; t < nthreads; ++t) pool.emplace_back(run, t, nthreads);
     for (auto& th : pool) th.join();
+  }
+  for (int s : row_status)
+    if (s) return s;
+  return 0;
+}
+
+// The layer-20 block pool (The Secret GPU Kernel Behind DeepSeek V4.1 Flash,
+// video transcript 7:22-7:46): the sweep that scores every position also
+// groups each row's valid prefix into blocks of `block` consecutive
+// positions (the last block may be short), gives every block the largest
+// score inside it, and keeps `pool` blocks: the `pinned` newest blocks (the
+// highest block indices) always, and the best-scoring other blocks (value
+// descending in the order above, ties to the smaller block index) until
+// `pool` blocks are kept or none is left.  Output per row: the kept block
+// indices in ascending order, padded with -1 to `pool` entries.
+//
+// Readings: the pages give blocks of eight and a pool of about 2,000
+// blocks (16,000 positions) but not how many blocks are pinned, so that is
+// a parameter; the pool is a set (upper indexers score inside it), emitted
+// as ascending block indices.
+//
+// Returns 0, 1 on a bad shape (as oracle_topk, plus block < 1, pool < 1,
+// pinned < 0, pinned > pool, pool - pinned > 2048), 2 on a null pointer,
+// 5 if a row held a NaN (that row's pool is all -1), 6 on a bad length.
+int oracle_block_pool(const float* scores, int32_t rows, int64_t n,
+                      int64_t row_stride, const int32_t* lengths, int32_t block,
+                      int32_t pool, int32_t pinned, int32_t* out,
+                      int32_t nthreads) {
+  if (rows < 0 || n < 1 || n > INT32_MAX || row_stride < n || block < 1 ||
+      pool < 1 || pinned < 0 || pinned > pool || pool - pinned > 2048)
+    return 1;
+  if (rows == 0) return 0;
+  if (!scores || !out) return 2;
+  if (lengths) {
+    for (int32_t r = 0; r < rows; ++r)
+      if (lengths[r] < 0 || lengths[r] > n) return 6;
+  }
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > rows) nthreads = rows;
+  std::vector<int> row_status(static_cast<size_t>(rows), 0);
+  auto run = [&](int32_t first, int32_t step) {
+    for (int32_t r = first; r < rows; r += step) {
+      const int64_t len = lengths ? lengths[r] : n;
+      row_status[r] = pool_row(scores + static_cast<int64_t>(r) * row_stride, len, block,
+                               pool, pinned, out + static_cast<int64_t>(r) * pool);
+    }
+  };
+  if (nthreads == 1) {
+    run(0, 1);
+  } else {
+    std::vector<std::thread> th;
+    for (int32_t t = 0; t < nthreads; ++t) th.emplace_back(run, t, nthreads);
+    for (auto& t : th) t.join();
   }
   for (int s : row_status)
     if (s) return s;

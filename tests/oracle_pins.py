@@ -283,7 +283,122 @@ def pin_contract_errors(orc):
     assert orc.topk(y, 4, lengths=np.array([16, 5], np.int32))[2] == 0
 
 
+# ---- the block pool (layer-20 sweep, video transcript 7:22-7:46) ----------
+#
+# Blocks of `block` consecutive positions of the valid prefix (the last one
+# may be short) score the largest value inside them; the pool keeps the
+# `pinned` newest blocks and then the best other blocks (value descending,
+# ties to the smaller block index), emitted as ascending block indices padded
+# with -1.  Stated again here in plain Python with the order key above.
+
+def pool_brute_force(row, block, pool, pinned):
+    L = len(row)
+    nb = -(-L // block)
+    pe = min(pinned, nb)
+    cand = list(range(nb - pe))
+    score = {b: max((row[i] for i in range(b * block, min(L, (b + 1) * block))), key=_key)
+             for b in cand}
+    kept = set(range(nb - pe, nb))
+    left = list(cand)
+    while len(kept) < pool and left:
+        # the block no other remaining block beats
+        best = next(b for b in left
+                    if all(_key(score[b]) > _key(score[c]) or
+                           (_key(score[b]) == _key(score[c]) and b < c) for c in left if c != b))
+        left.remove(best)
+        kept.add(best)
+    out = sorted(kept)
+    return out + [-1] * (pool - len(out))
+
+
+def pin_pool_brute_force(orc, cases=150, seed=17):
+    rng = np.random.default_rng(seed)
+    for c in range(cases):
+        block = int(rng.choice([1, 2, 3, 8]))
+        L = int(rng.integers(0, 33))
+        pool = int(rng.integers(1, 7))
+        pinned = int(rng.integers(0, pool + 1))
+        row = [float(ALPHABET[j]) for j in rng.integers(0, len(ALPHABET), size=L)]
+        n = max(L, 1)
+        x = np.full((1, n), 7.0, dtype=np.float32)     # past the length: ignored
+        x[0, :L] = np.array(row, dtype=np.float32)
+        got, st = orc.block_pool(x, block, pool, pinned, lengths=np.array([L], np.int32), n=n)
+        assert st == 0
+        want = pool_brute_force(row, block, pool, pinned)
+        assert list(got[0]) == want, f"pool case {c}: {list(got[0])} != {want} (block {block}, L {L}, pool {pool}, pinned {pinned}, row {row})"
+
+
+def pin_pool_closed_forms(orc, seed=18):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((3, 1000)).astype(np.float32)
+    nb = 125
+    # a pool at least as large as the row: every block, ascending
+    got, st = orc.block_pool(x, 8, 200, 10)
+    assert st == 0 and all(list(r) == list(range(nb)) + [-1] * 75 for r in got)
+    # every place pinned: the newest blocks only
+    got, st = orc.block_pool(x, 8, 40, 40)
+    assert st == 0 and all(list(r) == list(range(nb - 40, nb)) for r in got)
+    # ascending rows: the best blocks are the newest ones anyway
+    asc = np.sort(x, axis=1)
+    got, st = orc.block_pool(asc, 8, 30, 3)
+    assert st == 0 and all(list(r) == list(range(nb - 30, nb)) for r in got)
+    # descending rows, nothing pinned: the oldest blocks
+    got, st = orc.block_pool(asc[:, ::-1].copy(), 8, 30, 0)
+    assert st == 0 and all(list(r) == list(range(30)) for r in got)
+    # one large score per chosen block, zeros elsewhere: exactly those blocks
+    y = np.zeros((1, 1000), np.float32)
+    chosen = [3, 17, 40, 41, 99]
+    for j, b in enumerate(chosen):
+        y[0, 8 * b + (j % 8)] = 10.0 + j
+    got, st = orc.block_pool(y, 8, 6, 1)
+    assert st == 0 and list(got[0]) == sorted(chosen) + [124]
+
+
+def pin_pool_invariants(orc, seed=19):
+    rng = np.random.default_rng(seed)
+    rows, n, block, pool, pinned = 4, 5000, 8, 100, 10
+    x = rng.standard_normal((rows, n)).astype(np.float32)
+    x[1] = np.round(x[1] * 2)                     # ties between blocks
+    lengths = np.array([5000, 4999, 17, 801], np.int32)
+    got, st = orc.block_pool(x, block, pool, pinned, lengths=lengths)
+    assert st == 0
+    for r in range(rows):
+        L = int(lengths[r])
+        nb = -(-L // block)
+        pe = min(pinned, nb)
+        kept = [int(b) for b in got[r] if b >= 0]
+        assert kept == sorted(set(kept)), "ascending and unique"
+        assert all(0 <= b < nb for b in kept)
+        assert len(kept) == min(pool, nb)
+        assert set(range(nb - pe, nb)) <= set(kept), "the newest blocks are pinned"
+        score = {b: max((float(v) for v in x[r, b * block:min(L, (b + 1) * block)]), key=_key)
+                 for b in range(nb)}
+        sel = [b for b in kept if b < nb - pe]
+        out = [b for b in range(nb - pe) if b not in set(kept)]
+        for b in sel:            # every chosen block beats every left-out one
+            for c in out:
+                assert _key(score[b]) > _key(score[c]) or (_key(score[b]) == _key(score[c]) and b < c)
+
+
+def pin_pool_contract(orc):
+    x = np.zeros((2, 16), dtype=np.float32)
+    assert orc.block_pool(x, 0, 4, 0)[1] == 1
+    assert orc.block_pool(x, 8, 0, 0)[1] == 1
+    assert orc.block_pool(x, 8, 4, 5)[1] == 1
+    assert orc.block_pool(x, 8, 2100, 10)[1] == 1
+    assert orc.block_pool(x, 8, 2058, 10)[1] == 0
+    assert orc.block_pool(x, 8, 4, 1, lengths=np.array([3, 17], np.int32))[1] == 6
+    y = x.copy()
+    y[1, 5] = np.nan
+    out, st = orc.block_pool(y, 8, 4, 1)
+    assert st == 5 and np.all(out[1] == -1)
+
+
 ALL_PINS = [
+    pin_pool_brute_force,
+    pin_pool_closed_forms,
+    pin_pool_invariants,
+    pin_pool_contract,
     pin_brute_force_exhaustive,
     pin_brute_force_random,
     pin_repeated_argmax,

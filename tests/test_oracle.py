@@ -29,6 +29,11 @@ MUTANTS = {
     7: "row stride ignored",
     8: "-inf dropped from the selection",
     9: "+inf clamped to the largest finite value",
+    10: "block pool: a block scored by its first value",
+    11: "block pool: the oldest blocks pinned",
+    12: "block pool: ties between blocks to the larger index",
+    13: "block pool: the short last block dropped",
+    14: "block pool: pinned blocks also compete for the free places",
 }
 
 
