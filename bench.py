@@ -154,13 +154,26 @@ def run_gb300(args, world, rank, local):
     vals = torch.empty((rows, k), dtype=torch.float32, device=dev)
     idx = torch.empty((rows, k), dtype=torch.int32, device=dev)
     split = B.topk_split_plan(rows, n)
-    ws = torch.zeros(B.topk_ws_bytes(rows, n, k), dtype=torch.uint8, device=dev)
+    pool = None
+    if args.pool:
+        # the layer-20 block pool in the same pass: pool_blocks, pinned_blocks
+        pool = tuple(int(t) for t in args.pool.split(","))
+        ws = torch.zeros(B.topk_pool_ws_bytes(rows, n, k, *pool), dtype=torch.uint8, device=dev)
+        out_pool = torch.empty((rows, pool[0]), dtype=torch.int32, device=dev)
+    else:
+        ws = torch.zeros(B.topk_ws_bytes(rows, n, k), dtype=torch.uint8, device=dev)
+
+    def select(x):
+        if pool:
+            rc = B.topk_select_pool(x, rows, n, stride, lengths, k, vals, idx, pool[0], pool[1],
+                                    out_pool, ws, stream)
+        else:
+            rc = B.topk_select(x, rows, n, stride, lengths, k, vals, idx, ws, stream)
+        if rc != 0:
+            raise RuntimeError(f"selection returned {rc}")
 
     def step(i):
-        rc = B.topk_select(bufs[i % N_INPUT_BUFFERS], rows, n, stride, lengths, k, vals, idx,
-                           ws, stream)
-        if rc != 0:
-            raise RuntimeError(f"topk_select returned {rc}")
+        select(bufs[i % N_INPUT_BUFFERS])
 
     barrier = D.barrier
 
@@ -192,17 +205,18 @@ def run_gb300(args, world, rank, local):
     len_pin = None if w.lengths is None else torch.from_numpy(w.lengths).pin_memory()
     vals_h = torch.empty((rows, k), dtype=torch.float32).pin_memory()
     idx_h = torch.empty((rows, k), dtype=torch.int32).pin_memory()
+    pool_h = torch.empty((rows, pool[0]), dtype=torch.int32).pin_memory() if pool else None
     dev_in = bufs[0]
 
     def e2e_step():
         dev_in.copy_(host_pin, non_blocking=True)
         if len_pin is not None:
             lengths.copy_(len_pin, non_blocking=True)
-        rc = B.topk_select(dev_in, rows, n, stride, lengths, k, vals, idx, ws, stream)
-        if rc != 0:
-            raise RuntimeError(f"topk_select returned {rc}")
+        select(dev_in)
         vals_h.copy_(vals, non_blocking=True)
         idx_h.copy_(idx, non_blocking=True)
+        if pool:
+            pool_h.copy_(out_pool, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -218,7 +232,7 @@ def run_gb300(args, world, rank, local):
     e2e_ms = D.max_over_ranks(e0.elapsed_time(e1), device=dev)
     e2e_value = world * rows / (e2e_ms / args.steps / 1e3)
     h2d = host.numel() * 4 + (0 if w.lengths is None else rows * 4)
-    d2h = rows * k * 8
+    d2h = rows * k * 8 + (rows * pool[0] * 4 if pool else 0)
 
     # Survivor counters for one call (elements that reached a tray sort).
     B.topk_ws_stats(ws, rows, n, k, 0, stream)
@@ -246,11 +260,11 @@ def run_gb300(args, world, rank, local):
         torch.cuda.synchronize()
         tk_ms = a.elapsed_time(b) / reps
 
-    alg_bytes = w.algorithmic_bytes()
+    alg_bytes = w.algorithmic_bytes() + (rows * pool[0] * 4 if pool else 0)
     avg_launch_ms = local_ms / args.steps
     peak, peak_kind = _peaks()
     achieved = alg_bytes / (avg_launch_ms / 1e3) / 1e9
-    traffic = _traffic_per_launch(args.workload)
+    traffic = None if pool else _traffic_per_launch(args.workload)
     T = k + 2 * 1024
     m = (n + 1023) // 1024
     harmonic = sum(1.0 / j for j in range(1, m + 1))
@@ -276,6 +290,8 @@ def run_gb300(args, world, rank, local):
             "l2": f"{N_INPUT_BUFFERS} rotating input buffers of "
                   f"{host.numel() * 4 / 2**20:.0f} MiB (> 129 MB L2), no flush",
             "parallelism": f"weak: {world} GPU(s), each its own batch",
+            **({"pool_blocks": pool[0], "pinned_blocks": pool[1],
+                "pool_block_positions": 8} if pool else {}),
         },
         "gbs": round(alg_bytes / (ms_per_step / 1e3) / 1e9, 1),
         "roofline": {
@@ -287,16 +303,17 @@ def run_gb300(args, world, rank, local):
             "traffic": traffic,
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
-            "kernel": "topk_select_kernel",
+            "kernel": "topk_select_kernel" + (" (+ pool_select_kernel)" if pool else ""),
             "algorithmic_bytes_per_launch": alg_bytes,
             "avg_launch_ms": round(avg_launch_ms, 5),
         },
         "e2e": {
             "value": round(e2e_value, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "pinned host -> device copy, topk_select (C ABI), device -> pinned host",
+            "path": "pinned host -> device copy, " + ("topk_select_pool" if pool else "topk_select") +
+                    " (C ABI), device -> pinned host",
         },
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if pool else 1),
         "clocks": clocks.summary(),
         "survivors": {
             "mean_per_row": round(float(np.mean(surv)), 1), "max_per_row": int(max(surv)),
@@ -390,6 +407,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="c4_normal_k512", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--pool", default=None,
+                    help="POOL,PINNED: also build the layer-20 block pool in the same pass "
+                         "(topk_select_pool; e.g. 2048,64)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=16)
     args = ap.parse_args()

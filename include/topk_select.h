@@ -77,6 +77,9 @@ extern "C" {
 /* Largest supported k. */
 #define TOPK_MAX_K 2048
 
+/* Positions per block of the layer-20 block pool (topk_select_pool). */
+#define TOPK_POOL_BLOCK 8
+
 /*
  * topk_ws_bytes -- workspace size, in bytes, that topk_select needs for this
  * shape (with the automatic split plan).  Returns 0 for an invalid shape.
@@ -221,6 +224,44 @@ int topk_select_noalloc(const float* scores, int32_t rows, int64_t n,
                         int64_t row_stride, const int32_t* lengths_or_null,
                         int32_t k, float* out_vals, int32_t* out_idx,
                         uint32_t* status_or_null, void* stream);
+
+/*
+ * topk_select_pool -- topk_select plus the layer-20 block pool, in the same
+ * pass over the scores.  The sweep that scores every position also groups
+ * them into blocks of eight, gives each block the best score inside it,
+ * keeps the best blocks with the newest ones pinned in, and upper indexers
+ * score only inside that pool (The Secret GPU Kernel Behind DeepSeek V4.1
+ * Flash, video transcript 7:22-7:46: about 2,000 blocks, 16,000 positions).
+ *
+ *   Per row r, with L_r its valid length: blocks b = 0 .. ceil(L_r / 8) - 1
+ *   cover positions [8b, min(8b + 8, L_r)); a block's score is the largest of
+ *   its scores (order as for topk_select: +0.0 above -0.0; NaN left out).
+ *   The pool keeps the min(pinned_blocks, #blocks) newest blocks (the highest
+ *   block indices) and fills the rest of its pool_blocks places with the
+ *   best-scoring other blocks (score descending, ties to the smaller block
+ *   index) while any is left.  out_pool[r * pool_blocks + j]: the kept block
+ *   indices in ascending order, then -1.  Block b stands for positions
+ *   8b .. 8b + 7 (those below L_r).
+ *
+ *   out_vals / out_idx: exactly as topk_select.  pool_blocks >= 1,
+ *   0 <= pinned_blocks <= pool_blocks, pool_blocks - pinned_blocks <=
+ *   TOPK_MAX_K.  out_pool: device int32[rows * pool_blocks], caller-owned.
+ *   ws: device workspace of topk_pool_ws_bytes(...) bytes, 256-byte aligned,
+ *   zero before the first call (the library leaves it so); its first word is
+ *   the status word (topk_ws_status).  A row holding a NaN sets
+ *   TOPK_STATUS_NAN; that row's pool is then unspecified.
+ *
+ * Returns TOPK_OK, TOPK_ERR_SHAPE, TOPK_ERR_ARG (pool arguments),
+ * TOPK_ERR_NULL, TOPK_ERR_WS or TOPK_ERR_LAUNCH.  Enqueues two kernels on
+ * `stream` (the selection, which also writes every block's maximum to the
+ * workspace, then one CTA per row that picks the pool); allocates nothing.
+ */
+size_t topk_pool_ws_bytes(int32_t rows, int64_t n, int32_t k, int32_t pool_blocks,
+                          int32_t pinned_blocks);
+int topk_select_pool(const float* scores, int32_t rows, int64_t n, int64_t row_stride,
+                     const int32_t* lengths_or_null, int32_t k, float* out_vals,
+                     int32_t* out_idx, int32_t pool_blocks, int32_t pinned_blocks,
+                     int32_t* out_pool, void* ws, void* stream);
 
 #ifdef __cplusplus
 }

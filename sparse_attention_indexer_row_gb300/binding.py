@@ -25,6 +25,7 @@ TOPK_STATUS_NAN = 1
 TOPK_STATUS_BAD_LENGTH = 2
 TOPK_STATUS_TIMEOUT = 4
 TOPK_STATUS_RESCAN = 8
+TOPK_POOL_BLOCK = 8
 TOPK_FLAG_IDENTITY_ORDER = 1
 TOPK_MAX_K = 2048
 
@@ -42,6 +43,9 @@ SIGNATURES = {
     "topk_ws_stats": (ctypes.c_int, [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P]),
     "topk_visit_order": (ctypes.c_int, [_I32, _I32, _I64, _U64, _P, _P]),
     "topk_select_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _P, _P, _P, _P]),
+    "topk_pool_ws_bytes": (_SZ, [_I32, _I64, _I32, _I32, _I32]),
+    "topk_select_pool": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _P, _P, _I32, _I32,
+                                        _P, _P, _P]),
 }
 
 
@@ -160,3 +164,14 @@ class TopK:
         if rc != TOPK_OK:
             raise RuntimeError(f"topk_select_ex returned {rc}")
         return self.vals, self.idx
+
+
+def topk_pool_ws_bytes(rows: int, n: int, k: int, pool_blocks: int, pinned_blocks: int) -> int:
+    return int(LIB.topk_pool_ws_bytes(rows, n, k, pool_blocks, pinned_blocks))
+
+
+def topk_select_pool(scores, rows, n, row_stride, lengths_or_null, k, out_vals, out_idx,
+                     pool_blocks, pinned_blocks, out_pool, ws, stream=None) -> int:
+    return int(LIB.topk_select_pool(_ptr(scores), rows, n, row_stride, _ptr(lengths_or_null), k,
+                                    _ptr(out_vals), _ptr(out_idx), pool_blocks, pinned_blocks,
+                                    _ptr(out_pool), _ptr(ws), _stream(stream)))

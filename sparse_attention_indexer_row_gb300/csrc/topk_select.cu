@@ -258,6 +258,8 @@ struct Params {
   uint64_t* partials;
   uint32_t seed_lo, seed_hi;
   uint32_t flags;
+  float* bmax;        // block pool: block maxima per row (null: not asked for)
+  int64_t bstride;    // block pool: row stride of bmax, in blocks
 };
 
 // What the producer tells the filters about a stage.
@@ -1047,6 +1049,35 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
   return ok;
 }
 
+// The layer-20 block pool's block maxima, computed in the same pass (The
+// Secret GPU Kernel Behind DeepSeek V4.1 Flash, video transcript 7:22-7:46):
+// a block is eight consecutive positions, i.e. a filter thread's float4 and
+// the next lane's; its score is the largest of its valid scores (NaN left
+// out; NaN only when every valid score is NaN), +0.0 above -0.0.  Lanes with
+// an even thread index store one float per block of the stage.
+__device__ __forceinline__ void store_block_max(const float (&x)[kEPT], uint32_t valid, int ft,
+                                                uint32_t e0, uint32_t nvalid, float* brow) {
+#pragma unroll
+  for (int u = 0; u < kF4; ++u) {
+    float v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      v[c] = ((valid >> (4 * u + c)) & 1u) ? x[4 * u + c] : __int_as_float(0x7FC00000);
+    const float m = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));  // (fmaxf skips a NaN)
+    float bm = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    if (__any_sync(0xFFFFFFFFu, bm == 0.0f)) {
+      // a zero maximum: +0.0 if the block holds a +0.0, else -0.0
+      bool pz = false;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) pz |= __float_as_uint(v[c]) == 0u;
+      pz |= __shfl_xor_sync(0xFFFFFFFFu, pz ? 1u : 0u, 1) != 0u;
+      if (bm == 0.0f) bm = pz ? 0.0f : -0.0f;
+    }
+    const uint32_t off = uint32_t(4 * (ft + kNFT * u));  // the float4's first element in the unit
+    if ((ft & 1) == 0 && off < nvalid) brow[(e0 + off) >> 3] = bm;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The selection kernel.
 
@@ -1294,6 +1325,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       const uint32_t copied = aligned ? (nvalid & ~3u) : 0u;
       float x[kEPT];
       const uint32_t valid = load_share(x, src, row, e0, nvalid, copied, ft);  // bit e: in the row
+      if (p.bmax != nullptr) store_block_max(x, valid, ft, e0, nvalid, p.bmax + int64_t(r) * p.bstride);
       // Most stages have no element past the threshold: the test first folds
       // each float4 group into one bit (a superset: it also passes NaN, ties
       // and padding); only flagged groups are re-read (where they sit: the
@@ -1998,6 +2030,217 @@ int32_t resolve_split(int32_t rows, int64_t n, int32_t split) {
   return split == 0 ? auto_split(rows, n) : split;
 }
 
+// ---------------------------------------------------------------------------
+// The layer-20 block pool around the selection (topk_select_pool).
+
+constexpr int kPoolBlock = TOPK_POOL_BLOCK;  // positions per block
+
+bool pool_args_ok(int32_t pool_blocks, int32_t pinned_blocks) {
+  return pool_blocks >= 1 && pinned_blocks >= 0 && pinned_blocks <= pool_blocks &&
+         pool_blocks - pinned_blocks <= TOPK_MAX_K;
+}
+
+// Workspace of topk_select_pool: the selection's own workspace first (its
+// status word is the call's), then the block maxima (rows x bstride floats).
+struct PoolLayout {
+  int64_t nb, bstride;
+  size_t bmax, total;
+};
+
+PoolLayout pool_layout(int32_t rows, int64_t n, int32_t k) {
+  PoolLayout L;
+  L.nb = (n + kPoolBlock - 1) / kPoolBlock;
+  L.bstride = (L.nb + 3) & ~int64_t(3);  // 16-byte aligned rows
+  L.bmax = align256(topk_ws_bytes_ex(rows, n, k, 0));
+  L.total = align256(L.bmax + sizeof(float) * size_t(rows) * size_t(L.bstride));
+  return L;
+}
+
+__device__ __forceinline__ int64_t pool_row_length(const int32_t* lengths, int32_t r, int64_t n) {
+  if (!lengths) return n;
+  const int64_t L = lengths[r];
+  return L < 0 ? 0 : (L > n ? n : L);
+}
+
+constexpr int kPoolSelThreads = 1024;
+constexpr uint32_t kPoolSeg = 32 * kPoolSelThreads;  // blocks per output segment (one word a thread)
+
+// CTA-wide exclusive prefix sum of one value per thread (kPoolSelThreads
+// threads); also returns the total.  Uses `scratch` (kPoolSelThreads / 32
+// words) and ends with a barrier.
+__device__ __forceinline__ uint32_t pool_scan(uint32_t v, uint32_t* scratch, uint32_t& total) {
+  const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) scratch[wp] = incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int q = 0; q < kPoolSelThreads / 32; ++q) {
+    const uint32_t c = scratch[q];
+    before += q < wp ? c : 0u;
+    all += c;
+  }
+  __syncthreads();
+  total = all;
+  return before + incl - v;
+}
+
+// One row's pool, one CTA per row: the best kb of the row's candidate blocks
+// (its blocks that are not pinned), found by a three-pass radix select on the
+// order key of each block maximum (12 + 12 + 8 bits; key 0: the block has no
+// score): the exact key T of the kb-th block and how many blocks equal to T
+// it takes, the first ones in index order.  The blocks above T and the first
+// of those equal to T are then written in ascending block order, then the
+// pinned blocks, then -1.
+__global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
+    const float* bmax, int64_t bstride, const int32_t* lengths, int64_t n, int32_t pool_blocks,
+    int32_t pinned, int32_t* out_pool) {
+  __shared__ uint32_t hist[4096];
+  __shared__ uint32_t gtbits[kPoolSelThreads], eqbits[kPoolSelThreads];
+  __shared__ uint32_t scratch[kPoolSelThreads / 32];
+  __shared__ uint32_t s_bin, s_above;
+  const int32_t r = blockIdx.x;
+  const int t = threadIdx.x;
+  const int64_t nb = (pool_row_length(lengths, r, n) + kPoolBlock - 1) / kPoolBlock;
+  const int32_t pe = int32_t(nb < pinned ? nb : pinned);
+  const uint32_t nc = uint32_t(nb - pe);  // candidate blocks [0, nc)
+  const uint32_t kb = uint32_t(pool_blocks - pe);
+  const float* row = bmax + int64_t(r) * bstride;
+  auto to_key = [](float v) -> uint32_t {
+    const uint32_t bits = __float_as_uint(v);
+    return (bits & 0x7FFFFFFFu) > 0x7F800000u ? 0u : order_key(bits);  // NaN: no score
+  };
+  // 16 keys a thread: four float4 loads in flight (row is 16-byte aligned)
+  auto load16 = [&](uint32_t base, uint32_t (&key)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t b = base + 4u * kPoolSelThreads * uint32_t(q) + 4u * uint32_t(t);
+      float4 v;
+      if (b + 4u <= nc) {
+        v = __ldg(reinterpret_cast<const float4*>(row + b));
+      } else {
+        const float nan = __int_as_float(0x7FC00000);
+        v.x = b < nc ? row[b] : nan;
+        v.y = b + 1u < nc ? row[b + 1u] : nan;
+        v.z = b + 2u < nc ? row[b + 2u] : nan;
+        v.w = b + 3u < nc ? row[b + 3u] : nan;
+      }
+      key[4 * q + 0] = to_key(v.x);
+      key[4 * q + 1] = to_key(v.y);
+      key[4 * q + 2] = to_key(v.z);
+      key[4 * q + 3] = to_key(v.w);
+    }
+  };
+  constexpr uint32_t kStep = 16u * kPoolSelThreads;
+
+  uint32_t prefix = 0, pmask = 0, need = kb;
+  bool all = false;
+  const int shifts[3] = {20, 8, 0};
+  const int widths[3] = {12, 12, 8};
+  for (int pass = 0; pass < 3 && kb > 0 && nc > 0; ++pass) {
+    const int sh = shifts[pass];
+    const uint32_t dmask = (1u << widths[pass]) - 1u;
+    for (int j = t; j < 4096; j += kPoolSelThreads) hist[j] = 0u;
+    __syncthreads();
+    for (uint32_t base = 0; base < nc; base += kStep) {
+      uint32_t key[16];
+      load16(base, key);
+      bool any = false;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) any |= key[q] != 0u && (key[q] & pmask) == prefix;
+      if (!__any_sync(0xFFFFFFFFu, any)) continue;  // (later passes: most warps)
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (key[q] != 0u && (key[q] & pmask) == prefix) atomicAdd(&hist[(key[q] >> sh) & dmask], 1u);
+    }
+    __syncthreads();
+    // bins from the top: thread t owns nbins / kPoolSelThreads of them (or one)
+    const int nbins = int(dmask) + 1;
+    const int per = nbins >= kPoolSelThreads ? nbins / kPoolSelThreads : 1;
+    const int top = nbins - 1 - t * per;
+    uint32_t mine = 0;
+    if (top >= 0)
+      for (int q = 0; q < per; ++q) mine += hist[top - q];
+    uint32_t total;
+    const uint32_t above = pool_scan(mine, scratch, total);
+    if (pass == 0 && total <= kb) {  // every scored candidate fits: take them all
+      all = true;
+      break;
+    }
+    if (top >= 0 && above < need && above + mine >= need) {
+      uint32_t acc = above;
+      for (int q = 0; q < per; ++q) {
+        const uint32_t c = hist[top - q];
+        if (acc + c >= need) {
+          s_bin = uint32_t(top - q);
+          s_above = acc;
+          break;
+        }
+        acc += c;
+      }
+    }
+    __syncthreads();
+    prefix |= s_bin << sh;
+    pmask |= dmask << sh;
+    need -= s_above;
+    __syncthreads();
+  }
+  // T: the kb-th block's key (0 when every scored candidate is taken);
+  // eq_take: how many blocks equal to T belong to the pool
+  const uint32_t T = (kb > 0 && nc > 0 && !all) ? prefix : 0u;
+  const uint32_t eq_take = (kb > 0 && nc > 0 && !all) ? need : 0u;
+
+  // Ascending output, one segment of kPoolSeg blocks at a time: a selected
+  // block's place = blocks above T before it + min(blocks equal to T before
+  // it, eq_take).
+  int32_t* out = out_pool + int64_t(r) * pool_blocks;
+  uint32_t gt_run = 0, eq_run = 0;
+  for (uint32_t s0 = 0; kb > 0 && s0 < nc; s0 += kPoolSeg) {
+    gtbits[t] = 0u;
+    eqbits[t] = 0u;
+    __syncthreads();
+    const uint32_t send = min(nc, s0 + kPoolSeg);
+    for (uint32_t base = s0; base < send; base += kStep) {
+      uint32_t key[16];
+      load16(base, key);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const uint32_t b = base + 4u * kPoolSelThreads * uint32_t(q >> 2) + 4u * uint32_t(t) +
+                           uint32_t(q & 3);
+        if (b < send && key[q] != 0u) {
+          const uint32_t w = (b - s0) >> 5, bit = 1u << ((b - s0) & 31u);
+          if (key[q] > T) atomicOr(&gtbits[w], bit);
+          else if (key[q] == T) atomicOr(&eqbits[w], bit);
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t g = gtbits[t], e = eqbits[t];
+    uint32_t tot;
+    const uint32_t before = pool_scan(uint32_t(__popc(g)) | (uint32_t(__popc(e)) << 16), scratch, tot);
+    const uint32_t gb = gt_run + (before & 0xFFFFu), eb = eq_run + (before >> 16);
+    // this word's equal blocks that are still within eq_take
+    uint32_t esel = 0u, left = eq_take > eb ? eq_take - eb : 0u;
+    for (uint32_t m = e; m != 0u && left > 0u; m &= m - 1u, --left) esel |= m & (0u - m);
+    uint32_t pos = gb + min(eb, eq_take);
+    for (uint32_t m = g | esel; m != 0u; m &= m - 1u)
+      out[pos++] = int32_t(s0 + 32u * uint32_t(t) + uint32_t(__ffs(m) - 1));
+    gt_run += tot & 0xFFFFu;
+    eq_run += tot >> 16;
+    __syncthreads();
+  }
+  const uint32_t sel = gt_run + min(eq_run, eq_take);
+  for (int j = t; j < pool_blocks; j += kPoolSelThreads) {
+    if (uint32_t(j) < sel) continue;
+    out[j] = uint32_t(j) < sel + uint32_t(pe) ? int32_t(nb - pe) + (j - int32_t(sel)) : -1;
+  }
+}
+
 }  // namespace
 }  // namespace topk
 
@@ -2093,9 +2336,12 @@ size_t topk_ws_bytes(int32_t rows, int64_t n, int32_t k) {
   return topk_ws_bytes_ex(rows, n, k, 0);
 }
 
-int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_stride,
-                   const int32_t* lengths_or_null, int32_t k, float* out_vals, int32_t* out_idx,
-                   void* ws, void* stream, int32_t split, uint64_t seed, uint32_t flags) {
+// The selection launch; `bmax` (block pool maxima, null for none) serves
+// topk_select_pool.
+static int launch_select(const float* scores, int32_t rows, int64_t n, int64_t row_stride,
+                         const int32_t* lengths_or_null, int32_t k, float* out_vals,
+                         int32_t* out_idx, void* ws, void* stream, int32_t split, uint64_t seed,
+                         uint32_t flags, float* bmax, int64_t bstride) {
   if (!shape_ok(rows, n, k) || row_stride < n || split < 0 || split > kMaxSplit)
     return TOPK_ERR_SHAPE;
   if (rows == 0) return TOPK_OK;
@@ -2126,6 +2372,8 @@ int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_str
   p.out_vals = out_vals;
   p.out_idx = out_idx;
   p.status = reinterpret_cast<uint32_t*>(w);
+  p.bmax = bmax;
+  p.bstride = bstride;
   p.tickets = reinterpret_cast<uint32_t*>(w + wl.tickets);
   p.survivors = reinterpret_cast<uint32_t*>(w + wl.survivors);
   p.sorts = reinterpret_cast<uint32_t*>(w + wl.sorts);
@@ -2163,11 +2411,47 @@ int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_str
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
 }
 
+int topk_select_ex(const float* scores, int32_t rows, int64_t n, int64_t row_stride,
+                   const int32_t* lengths_or_null, int32_t k, float* out_vals, int32_t* out_idx,
+                   void* ws, void* stream, int32_t split, uint64_t seed, uint32_t flags) {
+  return launch_select(scores, rows, n, row_stride, lengths_or_null, k, out_vals, out_idx, ws,
+                       stream, split, seed, flags, nullptr, 0);
+}
+
 int topk_select(const float* scores, int32_t rows, int64_t n, int64_t row_stride,
                 const int32_t* lengths_or_null, int32_t k, float* out_vals, int32_t* out_idx,
                 void* ws, void* stream) {
   return topk_select_ex(scores, rows, n, row_stride, lengths_or_null, k, out_vals, out_idx, ws,
                         stream, 0, kDefaultSeed, 0u);
+}
+
+size_t topk_pool_ws_bytes(int32_t rows, int64_t n, int32_t k, int32_t pool_blocks,
+                          int32_t pinned_blocks) {
+  if (!shape_ok(rows, n, k) || !pool_args_ok(pool_blocks, pinned_blocks)) return 0;
+  return pool_layout(rows, n, k).total;
+}
+
+int topk_select_pool(const float* scores, int32_t rows, int64_t n, int64_t row_stride,
+                     const int32_t* lengths_or_null, int32_t k, float* out_vals,
+                     int32_t* out_idx, int32_t pool_blocks, int32_t pinned_blocks,
+                     int32_t* out_pool, void* ws, void* stream) {
+  if (!shape_ok(rows, n, k) || row_stride < n) return TOPK_ERR_SHAPE;
+  if (!pool_args_ok(pool_blocks, pinned_blocks)) return TOPK_ERR_ARG;
+  if (rows == 0) return TOPK_OK;
+  if (!scores || !out_vals || !out_idx || !out_pool) return TOPK_ERR_NULL;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TOPK_ERR_WS;
+  const PoolLayout pl = pool_layout(rows, n, k);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  float* bmax = reinterpret_cast<float*>(w + pl.bmax);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // one pass over the scores: the top-k and every block's maximum
+  int rc = launch_select(scores, rows, n, row_stride, lengths_or_null, k, out_vals, out_idx, w,
+                         stream, 0, kDefaultSeed, 0u, bmax, pl.bstride);
+  if (rc != TOPK_OK) return rc;
+  // the best blocks among each row's blocks that are not pinned, and the pool
+  pool_select_kernel<<<rows, kPoolSelThreads, 0, st>>>(bmax, pl.bstride, lengths_or_null, n,
+                                                        pool_blocks, pinned_blocks, out_pool);
+  return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
 }
 
 int topk_ws_status(void* ws, uint32_t* status_out, void* stream) {
