@@ -155,6 +155,8 @@ __host__ __device__ inline int ring_stages(int kp) { return kp <= 512 ? 5 : 4; }
 // Plans.
 constexpr int kPlanItems = 0;  // (row, segment) items dealt round-robin to the grid
 constexpr int kPlanFlat = 1;   // equal shares of the batch's units
+constexpr int kPlanQueue = 2;  // (row, segment) items taken from a shared queue, longest rows first
+constexpr int kQueueMaxUnits = 4096;  // longest row (in units) the queue's order kernel sorts
 
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned):
@@ -164,6 +166,8 @@ constexpr int kPlanFlat = 1;   // equal shares of the batch's units
 //   sorts     u32[rows]   bitonic tray sorts per row
 //   admitted  u32[rows]   elements that passed the threshold test, per row
 //                         (the three counters accumulate until read)
+//   queue     u32[2]      queue plan: next item, CTAs done; zero between calls
+//   order     i32[rows]   queue plan: rows, longest first
 //   theta     u64[rows]   split rows: best threshold word any of the row's CTAs
 //                         has reached, zero between calls
 //   spec      u64[rows]   split rows: largest speculative threshold word any of
@@ -172,7 +176,7 @@ constexpr int kPlanFlat = 1;   // equal shares of the batch's units
 //                         max(rows * split, 2 * kMaxFlatCtas) when rows can
 //                         be split, else none
 struct WsLayout {
-  size_t tickets, survivors, sorts, admitted, theta, spec, partials, total;
+  size_t tickets, survivors, sorts, admitted, queue, order, theta, spec, partials, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -220,6 +224,10 @@ WsLayout ws_layout(int32_t rows, int32_t kp, size_t slots) {
   off = align256(off + sizeof(uint32_t) * size_t(rows));
   L.admitted = off;
   off = align256(off + sizeof(uint32_t) * size_t(rows));
+  L.queue = off;
+  off = align256(off + 2 * sizeof(uint32_t));
+  L.order = off;
+  off = align256(off + sizeof(int32_t) * size_t(rows));
   L.theta = off;
   off = align256(off + sizeof(uint64_t) * size_t(rows));
   L.spec = off;
@@ -242,9 +250,9 @@ struct Params {
   int32_t k;
   int32_t kp;         // next power of two >= k: kept-list capacity
   int32_t nstage;     // ring stages
-  int32_t plan;       // kPlanItems or kPlanFlat
-  int32_t split;      // kPlanItems: segments per row
-  int32_t seg_units;  // kPlanItems: units per segment
+  int32_t plan;       // kPlanItems, kPlanFlat or kPlanQueue
+  int32_t split;      // items and queue plans: segments per row
+  int32_t seg_units;  // items and queue plans: units per segment
   int32_t u_full;     // units per full row
   float* out_vals;
   int32_t* out_idx;
@@ -258,6 +266,8 @@ struct Params {
   uint64_t* partials;
   uint32_t seed_lo, seed_hi;
   uint32_t flags;
+  uint32_t* queue;    // queue plan: next item, CTAs done
+  const int32_t* order;  // queue plan: rows, longest first (null: index order)
   float* bmax;        // block pool: block maxima per row (null: not asked for)
   int64_t bstride;    // block pool: row stride of bmax, in blocks
 };
@@ -351,16 +361,42 @@ __device__ __forceinline__ int32_t flat_cta_of(int64_t b, int64_t M, int64_t G) 
   return int32_t(((b + 1) * G - 1) / M);
 }
 
+// The next item of the queue plan's shared queue, taken by lane 0 for the
+// warp; `total` or more means the queue is empty.  The last CTA to find it
+// empty resets it for the next call (every other CTA has stopped taking
+// items by then).  Kept out of line: it runs once per piece.
+__device__ __noinline__ uint32_t queue_take(uint32_t* queue, uint32_t total) {
+  uint32_t q = 0;
+  if ((threadIdx.x & 31) == 0) {
+    q = atomicAdd(queue, 1u);
+    if (q >= total) {
+      __threadfence();
+      if (atomicAdd(queue + 1, 1u) == gridDim.x - 1u) {
+        atomicExch(queue, 0u);
+        atomicExch(queue + 1, 0u);
+      }
+    }
+  }
+  return __shfl_sync(0xFFFFFFFFu, q, 0);
+}
+
 // The pi-th piece of this CTA: 0 = no more pieces, 1 = a piece, 2 = an
 // empty item to skip (a segment past the end of a short row).
 __device__ int get_piece(const Params& p, int32_t pi, Piece& out, bool& bad_len) {
   const int64_t cta = blockIdx.x;
   const int64_t G = gridDim.x;
   bad_len = false;
-  if (p.plan == kPlanItems) {
-    const int64_t item = cta + int64_t(pi) * G;
-    if (item >= int64_t(p.rows) * p.split) return 0;
-    const int32_t r = int32_t(item / p.split);
+  if (p.plan == kPlanItems || p.plan == kPlanQueue) {
+    const int64_t total = int64_t(p.rows) * p.split;
+    int64_t item;
+    if (p.plan == kPlanItems) {
+      item = cta + int64_t(pi) * G;  // dealt round-robin
+    } else {
+      item = int64_t(queue_take(p.queue, uint32_t(total)));
+    }
+    if (item >= total) return 0;
+    const int32_t rank = int32_t(item / p.split);
+    const int32_t r = p.order ? p.order[rank] : rank;
     const int32_t s = int32_t(item % p.split);
     int64_t L = p.lengths ? int64_t(p.lengths[r]) : p.n;
     if (L < 0 || L > p.n) {
@@ -1883,7 +1919,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             const int i = gathered + stt;
             const int o = i + (i >= pc.self ? 1 : 0);  // contributor index
             int64_t slot;
-            if (p.plan == kPlanItems) {
+            if (p.plan != kPlanFlat) {  // items or queue: slot r * split + segment
               slot = int64_t(pc.r) * p.split + o;
             } else {
               const int64_t M = int64_t(p.rows) * p.u_full, G = gridDim.x;
@@ -2241,6 +2277,42 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
   }
 }
 
+// The queue plan's order: rows sorted by unit count, longest first (a
+// counting sort; rows of equal length in any order -- results never depend
+// on the order).  One CTA; unit counts up to kQueueMaxUnits.
+__global__ void __launch_bounds__(kPoolSelThreads) queue_order_kernel(
+    const int32_t* lengths, int32_t rows, int64_t n, int32_t u_full, int32_t* order) {
+  __shared__ uint32_t cnt[kQueueMaxUnits + 1];
+  __shared__ uint32_t scratch[kPoolSelThreads / 32];
+  const int t = threadIdx.x;
+  for (int j = t; j <= u_full; j += kPoolSelThreads) cnt[j] = 0u;
+  __syncthreads();
+  auto bin = [&](int32_t r) -> int {  // longest first: bin 0 holds the longest rows
+    const int64_t L = pool_row_length(lengths, r, n);
+    return u_full - int((L + kUnit - 1) / kUnit);
+  };
+  for (int32_t r = t; r < rows; r += kPoolSelThreads) atomicAdd(&cnt[bin(r)], 1u);
+  __syncthreads();
+  constexpr int kPer = (kQueueMaxUnits + 1 + kPoolSelThreads - 1) / kPoolSelThreads;
+  uint32_t c[kPer], sum = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int j = t * kPer + q;
+    c[q] = j <= u_full ? cnt[j] : 0u;
+    sum += c[q];
+  }
+  uint32_t total;
+  uint32_t off = pool_scan(sum, scratch, total);  // (ends with a barrier)
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int j = t * kPer + q;
+    if (j <= u_full) cnt[j] = off;
+    off += c[q];
+  }
+  __syncthreads();
+  for (int32_t r = t; r < rows; r += kPoolSelThreads) order[atomicAdd(&cnt[bin(r)], 1u)] = r;
+}
+
 }  // namespace
 }  // namespace topk
 
@@ -2400,12 +2472,23 @@ static int launch_select(const float* scores, int32_t rows, int64_t n, int64_t r
     p.plan = kPlanFlat;
     p.split = 1;
   } else {
-    // (row, segment) items dealt round-robin to one CTA per SM
+    // (row, segment) items for one CTA per SM: dealt round-robin, or, for
+    // batches of many rows, taken from a shared queue with the longest rows
+    // first (a CTA that drew short rows takes more of them)
     const int64_t items = int64_t(rows) * S;
     G = items < cap ? items : cap;
-    p.plan = kPlanItems;
+    p.plan = rows >= kManyRows ? kPlanQueue : kPlanItems;
   }
   if (G < 1) G = 1;
+  p.queue = reinterpret_cast<uint32_t*>(w + wl.queue);
+  p.order = nullptr;
+  if (p.plan == kPlanQueue && lengths_or_null && u_full <= kQueueMaxUnits) {
+    int32_t* order = reinterpret_cast<int32_t*>(w + wl.order);
+    queue_order_kernel<<<1, kPoolSelThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        lengths_or_null, rows, n, int32_t(u_full), order);
+    if (cudaGetLastError() != cudaSuccess) return TOPK_ERR_LAUNCH;
+    p.order = order;
+  }
   topk_select_kernel<<<unsigned(G), kThreads, smem_layout(kp).total,
                        static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
