@@ -1093,24 +1093,45 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
 // an even thread index store one float per block of the stage.
 __device__ __forceinline__ void store_block_max(const float (&x)[kEPT], uint32_t valid, int ft,
                                                 uint32_t e0, uint32_t nvalid, float* brow) {
+  float bm[kF4];
+  if (valid == 0xFFFFFFFFu) {  // a full unit: no element to leave out
 #pragma unroll
-  for (int u = 0; u < kF4; ++u) {
-    float v[4];
+    for (int u = 0; u < kF4; ++u) {
+      const float m = fmaxf(fmaxf(x[4 * u], x[4 * u + 1]), fmaxf(x[4 * u + 2], x[4 * u + 3]));
+      bm[u] = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // (fmaxf skips a NaN)
+    }
+  } else {
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      v[c] = ((valid >> (4 * u + c)) & 1u) ? x[4 * u + c] : __int_as_float(0x7FC00000);
-    const float m = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));  // (fmaxf skips a NaN)
-    float bm = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    if (__any_sync(0xFFFFFFFFu, bm == 0.0f)) {
-      // a zero maximum: +0.0 if the block holds a +0.0, else -0.0
+    for (int u = 0; u < kF4; ++u) {
+      float v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        v[c] = ((valid >> (4 * u + c)) & 1u) ? x[4 * u + c] : __int_as_float(0x7FC00000);
+      const float m = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+      bm[u] = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    }
+  }
+  bool zero = false;
+#pragma unroll
+  for (int u = 0; u < kF4; ++u) zero |= bm[u] == 0.0f;
+  if (__any_sync(0xFFFFFFFFu, zero)) {
+    // a zero maximum: +0.0 if the block holds a valid +0.0, else -0.0
+#pragma unroll
+    for (int u = 0; u < kF4; ++u) {
       bool pz = false;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) pz |= __float_as_uint(v[c]) == 0u;
+      for (int c = 0; c < 4; ++c)
+        pz |= ((valid >> (4 * u + c)) & 1u) && __float_as_uint(x[4 * u + c]) == 0u;
       pz |= __shfl_xor_sync(0xFFFFFFFFu, pz ? 1u : 0u, 1) != 0u;
-      if (bm == 0.0f) bm = pz ? 0.0f : -0.0f;
+      if (bm[u] == 0.0f) bm[u] = pz ? 0.0f : -0.0f;
     }
-    const uint32_t off = uint32_t(4 * (ft + kNFT * u));  // the float4's first element in the unit
-    if ((ft & 1) == 0 && off < nvalid) brow[(e0 + off) >> 3] = bm;
+  }
+  if ((ft & 1) == 0) {
+    // block of the float4 pair (ft, ft + 1) in group u: (e0 + 4 ft) / 8 + 128 u
+    float* dst = brow + ((e0 + 4u * uint32_t(ft)) >> 3);
+#pragma unroll
+    for (int u = 0; u < kF4; ++u)
+      if (uint32_t(4 * (ft + kNFT * u)) < nvalid) dst[(kNFT / 2) * u] = bm[u];
   }
 }
 
@@ -2038,6 +2059,15 @@ struct DeviceInfo {
 };
 DeviceInfo g_devices[64];
 
+// The block pool's kernel (defined below) and its launch shape.
+constexpr int kPoolSelThreads = 1024;
+constexpr uint32_t kPoolSeg = 32 * kPoolSelThreads;  // blocks per output segment (one word a thread)
+constexpr uint32_t kPoolCap = 8192;                  // keys the pool's fast path may collect
+constexpr int kPoolSmem = int(sizeof(uint32_t)) * (4096 + 2 * kPoolSelThreads + 2 * int(kPoolCap));
+__global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
+    const float* bmax, int64_t bstride, const int32_t* lengths, int64_t n, int32_t pool_blocks,
+    int32_t pinned, int32_t* out_pool);
+
 cudaError_t configure_device(int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -2050,6 +2080,9 @@ cudaError_t configure_device(int* sms) {
   int most = 0;
   for (int kp = 1; kp <= TOPK_MAX_K; kp <<= 1) most = max(most, smem_layout(kp).total);
   e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(pool_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kPoolSmem);
   if (e != cudaSuccess) return e;
   int count = 0;
   e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
@@ -2098,8 +2131,6 @@ __device__ __forceinline__ int64_t pool_row_length(const int32_t* lengths, int32
   return L < 0 ? 0 : (L > n ? n : L);
 }
 
-constexpr int kPoolSelThreads = 1024;
-constexpr uint32_t kPoolSeg = 32 * kPoolSelThreads;  // blocks per output segment (one word a thread)
 
 // CTA-wide exclusive prefix sum of one value per thread (kPoolSelThreads
 // threads); also returns the total.  Uses `scratch` (kPoolSelThreads / 32
@@ -2126,22 +2157,32 @@ __device__ __forceinline__ uint32_t pool_scan(uint32_t v, uint32_t* scratch, uin
   return before + incl - v;
 }
 
+
 // One row's pool, one CTA per row: the best kb of the row's candidate blocks
-// (its blocks that are not pinned), found by a three-pass radix select on the
-// order key of each block maximum (12 + 12 + 8 bits; key 0: the block has no
-// score): the exact key T of the kb-th block and how many blocks equal to T
-// it takes, the first ones in index order.  The blocks above T and the first
-// of those equal to T are then written in ascending block order, then the
-// pinned blocks, then -1.
+// (its blocks that are not pinned), by the order key of each block maximum
+// (key 0: the block has no score).  A radix select (12 + 12 + 8 bits) finds
+// the exact key T of the kb-th block and how many blocks equal to T the pool
+// takes (the first ones in index order); the blocks above T and those are
+// written in ascending block order, then the pinned blocks, then -1.
+//   Fast path: a sample (8 consecutive keys of every `stride`) gives a key
+// that about 1.5 kb + 8 * stride / 8 of the row's keys reach; one pass over
+// the row collects every key at or above it into shared memory, and the
+// select and the ordered write run on that list.  If the list holds fewer
+// than kb keys or overflows, the select and the write run over the whole row
+// (three passes and a marking pass).
 __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
     const float* bmax, int64_t bstride, const int32_t* lengths, int64_t n, int32_t pool_blocks,
     int32_t pinned, int32_t* out_pool) {
-  __shared__ uint32_t hist[4096];
-  __shared__ uint32_t gtbits[kPoolSelThreads], eqbits[kPoolSelThreads];
+  extern __shared__ __align__(16) uint32_t psm[];
+  uint32_t* hist = psm;                          // 4096 bins
+  uint32_t* gtbits = psm + 4096;                 // output bitmaps, one word a thread
+  uint32_t* eqbits = gtbits + kPoolSelThreads;
+  uint32_t* lkey = eqbits + kPoolSelThreads;     // fast path: keys (the sample, then the list)
+  uint32_t* lidx = lkey + kPoolCap;              // fast path: their block indices
   __shared__ uint32_t scratch[kPoolSelThreads / 32];
-  __shared__ uint32_t s_bin, s_above;
+  __shared__ uint32_t s_bin, s_above, s_n;
   const int32_t r = blockIdx.x;
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31;
   const int64_t nb = (pool_row_length(lengths, r, n) + kPoolBlock - 1) / kPoolBlock;
   const int32_t pe = int32_t(nb < pinned ? nb : pinned);
   const uint32_t nc = uint32_t(nb - pe);  // candidate blocks [0, nc)
@@ -2172,105 +2213,211 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
       key[4 * q + 3] = to_key(v.w);
     }
   };
+  auto block_of = [&](uint32_t base, int q) -> uint32_t {  // load16's key q
+    return base + 4u * kPoolSelThreads * uint32_t(q >> 2) + 4u * uint32_t(t) + uint32_t(q & 3);
+  };
   constexpr uint32_t kStep = 16u * kPoolSelThreads;
 
-  uint32_t prefix = 0, pmask = 0, need = kb;
-  bool all = false;
-  const int shifts[3] = {20, 8, 0};
-  const int widths[3] = {12, 12, 8};
-  for (int pass = 0; pass < 3 && kb > 0 && nc > 0; ++pass) {
-    const int sh = shifts[pass];
-    const uint32_t dmask = (1u << widths[pass]) - 1u;
-    for (int j = t; j < 4096; j += kPoolSelThreads) hist[j] = 0u;
-    __syncthreads();
-    for (uint32_t base = 0; base < nc; base += kStep) {
-      uint32_t key[16];
-      load16(base, key);
-      bool any = false;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) any |= key[q] != 0u && (key[q] & pmask) == prefix;
-      if (!__any_sync(0xFFFFFFFFu, any)) continue;  // (later passes: most warps)
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        if (key[q] != 0u && (key[q] & pmask) == prefix) atomicAdd(&hist[(key[q] >> sh) & dmask], 1u);
-    }
-    __syncthreads();
-    // bins from the top: thread t owns nbins / kPoolSelThreads of them (or one)
-    const int nbins = int(dmask) + 1;
-    const int per = nbins >= kPoolSelThreads ? nbins / kPoolSelThreads : 1;
-    const int top = nbins - 1 - t * per;
-    uint32_t mine = 0;
-    if (top >= 0)
-      for (int q = 0; q < per; ++q) mine += hist[top - q];
-    uint32_t total;
-    const uint32_t above = pool_scan(mine, scratch, total);
-    if (pass == 0 && total <= kb) {  // every scored candidate fits: take them all
-      all = true;
-      break;
-    }
-    if (top >= 0 && above < need && above + mine >= need) {
-      uint32_t acc = above;
-      for (int q = 0; q < per; ++q) {
-        const uint32_t c = hist[top - q];
-        if (acc + c >= need) {
-          s_bin = uint32_t(top - q);
-          s_above = acc;
-          break;
-        }
-        acc += c;
+  // One radix select: `feed(prefix, pmask, sh, dmask)` adds the keys that
+  // match the prefix into hist.  want >= 1.  Returns the key of the want-th
+  // largest (0 and all = true when every key is taken) and in need how many
+  // keys equal to it are taken.
+  auto radix = [&](auto feed, uint32_t want, uint32_t& T, uint32_t& need, bool& all) {
+    uint32_t prefix = 0, pmask = 0;
+    need = want;
+    all = false;
+    const int shifts[3] = {20, 8, 0};
+    const int widths[3] = {12, 12, 8};
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sh = shifts[pass];
+      const uint32_t dmask = (1u << widths[pass]) - 1u;
+      for (int j = t; j < 4096; j += kPoolSelThreads) hist[j] = 0u;
+      __syncthreads();
+      feed(prefix, pmask, sh, dmask);
+      __syncthreads();
+      const int nbins = int(dmask) + 1;
+      const int per = nbins >= kPoolSelThreads ? nbins / kPoolSelThreads : 1;
+      const int top = nbins - 1 - t * per;
+      uint32_t mine = 0;
+      if (top >= 0)
+        for (int q = 0; q < per; ++q) mine += hist[top - q];
+      uint32_t total;
+      const uint32_t above = pool_scan(mine, scratch, total);
+      if (pass == 0 && total <= want) {
+        all = true;
+        break;
       }
+      if (top >= 0 && above < need && above + mine >= need) {
+        uint32_t acc = above;
+        for (int q = 0; q < per; ++q) {
+          const uint32_t c = hist[top - q];
+          if (acc + c >= need) {
+            s_bin = uint32_t(top - q);
+            s_above = acc;
+            break;
+          }
+          acc += c;
+        }
+      }
+      __syncthreads();
+      prefix |= s_bin << sh;
+      pmask |= dmask << sh;
+      need -= s_above;
+      __syncthreads();
     }
-    __syncthreads();
-    prefix |= s_bin << sh;
-    pmask |= dmask << sh;
-    need -= s_above;
-    __syncthreads();
-  }
-  // T: the kb-th block's key (0 when every scored candidate is taken);
-  // eq_take: how many blocks equal to T belong to the pool
-  const uint32_t T = (kb > 0 && nc > 0 && !all) ? prefix : 0u;
-  const uint32_t eq_take = (kb > 0 && nc > 0 && !all) ? need : 0u;
+    T = all ? 0u : prefix;
+    if (all) need = 0u;
+  };
 
-  // Ascending output, one segment of kPoolSeg blocks at a time: a selected
-  // block's place = blocks above T before it + min(blocks equal to T before
-  // it, eq_take).
+  // Ascending output over segments of kPoolSeg blocks: `mark(s0, send)` sets
+  // the bits of the blocks above T (gtbits) and equal to T (eqbits); a
+  // selected block's place = blocks above T before it + min(blocks equal to
+  // T before it, eq_take).  Returns how many blocks were written.
   int32_t* out = out_pool + int64_t(r) * pool_blocks;
-  uint32_t gt_run = 0, eq_run = 0;
-  for (uint32_t s0 = 0; kb > 0 && s0 < nc; s0 += kPoolSeg) {
-    gtbits[t] = 0u;
-    eqbits[t] = 0u;
-    __syncthreads();
-    const uint32_t send = min(nc, s0 + kPoolSeg);
-    for (uint32_t base = s0; base < send; base += kStep) {
-      uint32_t key[16];
-      load16(base, key);
+  auto emit = [&](auto mark, uint32_t eq_take) -> uint32_t {
+    uint32_t gt_run = 0, eq_run = 0;
+    for (uint32_t s0 = 0; s0 < nc; s0 += kPoolSeg) {
+      gtbits[t] = 0u;
+      eqbits[t] = 0u;
+      __syncthreads();
+      mark(s0, min(nc, s0 + kPoolSeg));
+      __syncthreads();
+      const uint32_t g = gtbits[t], e = eqbits[t];
+      uint32_t tot;
+      const uint32_t before =
+          pool_scan(uint32_t(__popc(g)) | (uint32_t(__popc(e)) << 16), scratch, tot);
+      const uint32_t gb = gt_run + (before & 0xFFFFu), eb = eq_run + (before >> 16);
+      uint32_t esel = 0u, left = eq_take > eb ? eq_take - eb : 0u;
+      for (uint32_t m = e; m != 0u && left > 0u; m &= m - 1u, --left) esel |= m & (0u - m);
+      uint32_t pos = gb + min(eb, eq_take);
+      for (uint32_t m = g | esel; m != 0u; m &= m - 1u)
+        out[pos++] = int32_t(s0 + 32u * uint32_t(t) + uint32_t(__ffs(m) - 1));
+      gt_run += tot & 0xFFFFu;
+      eq_run += tot >> 16;
+      __syncthreads();
+    }
+    return gt_run + min(eq_run, eq_take);
+  };
+  auto set_bit = [&](uint32_t b, uint32_t s0, uint32_t key, uint32_t T) {
+    const uint32_t w = (b - s0) >> 5, bit = 1u << ((b - s0) & 31u);
+    if (key > T) atomicOr(&gtbits[w], bit);
+    else if (key == T) atomicOr(&eqbits[w], bit);
+  };
+
+  uint32_t sel = 0;
+  bool done = kb == 0 || nc == 0;
+  if (!done) {
+    // ---- fast path: sample, collect, select and write from the list ----
+    uint32_t stride = 128;
+    while (uint64_t(stride) * kPoolSelThreads < nc) stride <<= 1;  // one group a thread
+    const uint32_t ngroups = (nc + stride - 1) / stride;
+    if (ngroups * 8u <= kPoolCap) {
+      // sample: keys [g * stride, g * stride + 8) of group g
+      if (uint32_t(t) < ngroups) {
+        const uint32_t b0 = uint32_t(t) * stride;
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const uint32_t b = base + 4u * kPoolSelThreads * uint32_t(q >> 2) + 4u * uint32_t(t) +
-                           uint32_t(q & 3);
-        if (b < send && key[q] != 0u) {
-          const uint32_t w = (b - s0) >> 5, bit = 1u << ((b - s0) & 31u);
-          if (key[q] > T) atomicOr(&gtbits[w], bit);
-          else if (key[q] == T) atomicOr(&eqbits[w], bit);
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t b = b0 + uint32_t(c);
+          lkey[8 * t + c] = b < nc ? to_key(row[b]) : 0u;
         }
       }
+      __syncthreads();
+      const uint32_t scount = ngroups * 8u;
+      // the sample key that about 1.5 kb + stride of the row's keys reach
+      const uint64_t want64 = (3ull * kb * 8ull + 2ull * stride - 1ull) / (2ull * stride) + 8ull;
+      uint32_t T0 = 0, e0 = 0;
+      bool all0 = false;
+      if (want64 <= scount) {
+        radix([&](uint32_t prefix, uint32_t pmask, int sh, uint32_t dmask) {
+                for (uint32_t i = t; i < scount; i += kPoolSelThreads) {
+                  const uint32_t k = lkey[i];
+                  if (k != 0u && (k & pmask) == prefix) atomicAdd(&hist[(k >> sh) & dmask], 1u);
+                }
+              }, uint32_t(want64), T0, e0, all0);
+      }
+      // collect every key >= T0 (all keys when the sample cannot bound them)
+      if (t == 0) s_n = 0u;
+      __syncthreads();
+      const uint32_t lo = all0 || want64 > scount ? 1u : T0;
+      for (uint32_t base = 0; base < nc; base += kStep) {
+        uint32_t key[16];
+        load16(base, key);
+        uint32_t c = 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) c += (key[q] >= lo && block_of(base, q) < nc) ? 1u : 0u;
+        uint32_t incl = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+          if (lane >= d) incl += o;
+        }
+        uint32_t wbase = 0;
+        if (lane == 31 && incl) wbase = atomicAdd(&s_n, incl);
+        wbase = __shfl_sync(0xFFFFFFFFu, wbase, 31);
+        uint32_t at = wbase + incl - c;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const uint32_t b = block_of(base, q);
+          if (key[q] >= lo && b < nc) {
+            if (at < kPoolCap) {
+              lkey[at] = key[q];
+              lidx[at] = b;
+            }
+            ++at;
+          }
+        }
+      }
+      __syncthreads();
+      const uint32_t nl = s_n;
+      if (nl >= kb && nl <= kPoolCap) {
+        uint32_t T, eq_take;
+        bool all;
+        radix([&](uint32_t prefix, uint32_t pmask, int sh, uint32_t dmask) {
+                for (uint32_t i = t; i < nl; i += kPoolSelThreads) {
+                  const uint32_t k = lkey[i];
+                  if ((k & pmask) == prefix) atomicAdd(&hist[(k >> sh) & dmask], 1u);
+                }
+              }, kb, T, eq_take, all);
+        sel = emit([&](uint32_t s0, uint32_t send) {
+                     for (uint32_t i = t; i < nl; i += kPoolSelThreads) {
+                       const uint32_t b = lidx[i];
+                       if (b >= s0 && b < send) set_bit(b, s0, lkey[i], T);
+                     }
+                   }, eq_take);
+        done = true;
+      }
     }
-    __syncthreads();
-    const uint32_t g = gtbits[t], e = eqbits[t];
-    uint32_t tot;
-    const uint32_t before = pool_scan(uint32_t(__popc(g)) | (uint32_t(__popc(e)) << 16), scratch, tot);
-    const uint32_t gb = gt_run + (before & 0xFFFFu), eb = eq_run + (before >> 16);
-    // this word's equal blocks that are still within eq_take
-    uint32_t esel = 0u, left = eq_take > eb ? eq_take - eb : 0u;
-    for (uint32_t m = e; m != 0u && left > 0u; m &= m - 1u, --left) esel |= m & (0u - m);
-    uint32_t pos = gb + min(eb, eq_take);
-    for (uint32_t m = g | esel; m != 0u; m &= m - 1u)
-      out[pos++] = int32_t(s0 + 32u * uint32_t(t) + uint32_t(__ffs(m) - 1));
-    gt_run += tot & 0xFFFFu;
-    eq_run += tot >> 16;
-    __syncthreads();
   }
-  const uint32_t sel = gt_run + min(eq_run, eq_take);
+  if (!done) {
+    // ---- whole-row path ----
+    uint32_t T, eq_take;
+    bool all;
+    radix([&](uint32_t prefix, uint32_t pmask, int sh, uint32_t dmask) {
+            for (uint32_t base = 0; base < nc; base += kStep) {
+              uint32_t key[16];
+              load16(base, key);
+              bool any = false;
+#pragma unroll
+              for (int q = 0; q < 16; ++q) any |= key[q] != 0u && (key[q] & pmask) == prefix;
+              if (!__any_sync(0xFFFFFFFFu, any)) continue;
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+                if (key[q] != 0u && (key[q] & pmask) == prefix)
+                  atomicAdd(&hist[(key[q] >> sh) & dmask], 1u);
+            }
+          }, kb, T, eq_take, all);
+    sel = emit([&](uint32_t s0, uint32_t send) {
+                 for (uint32_t base = s0; base < send; base += kStep) {
+                   uint32_t key[16];
+                   load16(base, key);
+#pragma unroll
+                   for (int q = 0; q < 16; ++q) {
+                     const uint32_t b = block_of(base, q);
+                     if (b < send && key[q] != 0u) set_bit(b, s0, key[q], T);
+                   }
+                 }
+               }, eq_take);
+  }
   for (int j = t; j < pool_blocks; j += kPoolSelThreads) {
     if (uint32_t(j) < sel) continue;
     out[j] = uint32_t(j) < sel + uint32_t(pe) ? int32_t(nb - pe) + (j - int32_t(sel)) : -1;
@@ -2532,7 +2679,7 @@ int topk_select_pool(const float* scores, int32_t rows, int64_t n, int64_t row_s
                          stream, 0, kDefaultSeed, 0u, bmax, pl.bstride);
   if (rc != TOPK_OK) return rc;
   // the best blocks among each row's blocks that are not pinned, and the pool
-  pool_select_kernel<<<rows, kPoolSelThreads, 0, st>>>(bmax, pl.bstride, lengths_or_null, n,
+  pool_select_kernel<<<rows, kPoolSelThreads, kPoolSmem, st>>>(bmax, pl.bstride, lengths_or_null, n,
                                                         pool_blocks, pinned_blocks, out_pool);
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
 }
