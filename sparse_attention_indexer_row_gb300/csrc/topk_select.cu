@@ -103,7 +103,7 @@ static_assert(kWarmUnits <= 5, "warm-start units fit in the ring");
 // threshold those units only make likely (about 3.6 k words of the row above
 // it).  It is taken when they hold at least 2.5 k * sample / row length
 // elements at or above it, at most kSpecMaxNeed (so: long rows).
-constexpr uint32_t kSpecMaxNeed = 128;
+constexpr uint32_t kSpecMaxNeed = 256;
 constexpr int kRescanChunk = 2048;           // row elements a rescan step reads
 // Pre-final: when a piece of at least kPreFinalMin units is within kPreFinal
 // stages of its end, the selectors sort what they hold, so that its end only
@@ -344,7 +344,7 @@ struct CtaState {
   uint32_t est2[kNS];              // warm start: per selector warp candidate bound
   uint32_t warm_cnt;               // warm start: elements reaching the candidate
   uint32_t est3[kNS];              // warm start: per selector warp largest key
-  uint32_t spec_cnt[3];            // warm start: sample counts of the speculative bounds
+  uint32_t spec_cnt[5];            // warm start: sample counts of the speculative bounds
   uint32_t est4[kNS];              // warm start: per selector warp smallest unit maximum
   unsigned long long spec[2];      // speculative threshold word of the piece using inbox p
   const uint64_t* gsrc[16];        // leader merge: the partial lists of one gather step
@@ -733,8 +733,11 @@ struct Top4 {
   }
 };
 
-// For m > 64 the counts run over all 32 keys of each lane (one unit).
-__device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint32_t valid, int m) {
+// For m > 64 the counts run over all 32 keys of each lane (one unit).  The
+// bound resolves the key down to bit `low` (17: a 16-bit prefix; 1: the exact
+// m-th key).
+__device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint32_t valid, int m,
+                                                   int low = 17) {
   uint32_t key[kEPT];
   uint32_t ok = 0;
 #pragma unroll
@@ -746,7 +749,7 @@ __device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint3
   const uint32_t mm = uint32_t(m);
   uint32_t T = 0;
 #pragma unroll 1
-  for (int b = 31; b >= 17; b -= 2) {
+  for (int b = 31; b >= low; b -= 2) {
     const uint32_t t1 = T | (1u << (b - 1)), t2 = T | (2u << (b - 1)), t3 = T | (3u << (b - 1));
     uint32_t c12 = 0, c3 = 0;  // counts of at most 1024: two per word, sixteen bits each
 #pragma unroll
@@ -762,12 +765,20 @@ __device__ __forceinline__ uint32_t warp_key_bound(const float (&x)[kEPT], uint3
   return T;
 }
 
+// The sample count a speculative start needs (2.5 k * sample / row length).
+__host__ __device__ inline uint64_t spec_need(int k, int wu, uint32_t L) {
+  const uint64_t sample = uint64_t(wu) * uint64_t(kUnit);
+  return (5ull * uint64_t(k) * sample + 2ull * L - 1ull) / (2ull * L);
+}
+
 // Units a piece's warm start reads: kWarmUnits (at most the piece's units)
-// when each warp needs at most 64 elements (k <= 512), else one.
-__host__ __device__ inline int warm_units(int k, int nu) {
+// when each warp needs at most 64 elements (k <= 512); above that, four units
+// only where a speculative start may be taken (a long row), else one.
+__host__ __device__ inline int warm_units(int k, int nu, uint32_t L) {
   const int m = (k + kNS - 1) / kNS;
-  if (m > 64) return 1;
-  return nu < 1 ? 1 : (nu < kWarmUnits ? nu : kWarmUnits);
+  const int w = nu < 1 ? 1 : (nu < kWarmUnits ? nu : kWarmUnits);
+  if (m <= 64) return w;
+  return (w == kWarmUnits && L > 0u && spec_need(k, w, L) <= kSpecMaxNeed) ? w : 1;
 }
 
 // Warm start of piece w, whose first units have landed in the ring (the
@@ -788,7 +799,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
   const int m_warm = (k + kNS - 1) / kNS;
   bool ok = true;
   const Piece pw = st.table[w % kTable];
-  const int wu = warm_units(k, pw.u_end - pw.u_begin);
+  const int wu = warm_units(k, pw.u_end - pw.u_begin, pw.L);
   const float* wrow = scores + int64_t(pw.r) * row_stride;
   const bool waligned = (reinterpret_cast<uintptr_t>(wrow) & 15u) == 0;
   auto stage_of = [&](int q, const float*& src, StageDesc& d, uint32_t& copied) {
@@ -804,26 +815,34 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
   uint32_t mk = 0u;
   uint64_t spec = 0ull;  // speculative threshold word (0: none)
   bool decided = false;
-  // Speculative start (long pieces, k <= 512): the 8th, 7th and 6th largest
-  // of the selector warps' largest keys in the first unit are candidates;
+  uint32_t mk_floor = 0u;  // a proven bound from the speculative candidates
+  // Speculative start (pieces of long rows): the 8th, 7th and 6th largest of
+  // the selector warps' rank-R keys in the first unit are candidates (R = 1,
+  // the largest, for k <= 512; above, R makes the candidates' expected sample
+  // count about 1.25 need);
   // the highest one that the wu sample units hold at least `need` elements
   // at or above is taken (need = 2.5 k * sample / row length, so that the row
   // holds about 3.6 k above it).  The count is a strict float compare (it
   // never counts NaN, and misses only -0.0 against a +0.0 bound).  Only when
   // no candidate is supported do the lane lists below run.
   const int nu = pw.u_end - pw.u_begin;
-  if (m_warm <= 64 && wu == kWarmUnits && nu >= kWarmUnits) {
-    const uint64_t sample = uint64_t(wu) * uint64_t(kUnit);
-    const uint64_t need64 = (5ull * uint64_t(k) * sample + 2ull * pw.L - 1ull) / (2ull * pw.L);
+  if (wu == kWarmUnits && nu >= kWarmUnits) {
+    const uint64_t need64 = spec_need(k, wu, pw.L);
     if (need64 <= kSpecMaxNeed) {
       const uint32_t need = uint32_t(need64);
+      const int R = need <= 128u ? 1 : int((5u * need + 4u * wu * kNS - 1u) / (4u * wu * kNS));
       float lm = -__int_as_float(0x7F800000);
+      uint32_t wkey = 0u;  // this warp's rank-R key of the first unit
       {
         const float* src;
         StageDesc d;
         uint32_t copied;
         stage_of(0, src, d, copied);
-        if (copied == uint32_t(kUnit)) {
+        if (R > 1) {
+          float x[kEPT];
+          const uint32_t valid = load_share(x, src, wrow, d.e0, d.nvalid, copied, stt);
+          wkey = warp_key_bound(x, valid, R, 1);  // exact: a coarse bound could pass a whole top unit
+        } else if (copied == uint32_t(kUnit)) {
 #pragma unroll
           for (int u = 0; u < kF4; ++u) {
             const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
@@ -840,12 +859,14 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
           }
         }
       }
-      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, Top4::key_of(lm));
-      if (lane == 0) st.est3[swarp] = wmax;
+      if (R == 1) wkey = __reduce_max_sync(0xFFFFFFFFu, Top4::key_of(lm));
+      if (lane == 0) st.est3[swarp] = wkey;
       if (stt == 0) {
         st.spec_cnt[0] = 0u;
         st.spec_cnt[1] = 0u;
         st.spec_cnt[2] = 0u;
+        st.spec_cnt[3] = 0u;
+        st.spec_cnt[4] = 0u;
       }
       Sel::sync();
       // the three smallest warp maxima
@@ -863,6 +884,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
                     f6 = key_to_float(s6 - 1u);  // key >= s  <=>  value > key_to_float(s - 1)
         uint32_t ca = 0u, cb = 0u;               // counts: s8 | s7 << 16, and s6
         uint32_t umin = 0xFFFFFFFFu;             // smallest of this warp's unit maxima
+        uint32_t ca0 = 0u, cb0 = 0u;             // the first unit's share of the counts
         for (int q = 0; q < wu; ++q) {
           const float* src;
           StageDesc d;
@@ -896,29 +918,43 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
             }
           }
           umin = min(umin, __reduce_max_sync(0xFFFFFFFFu, Top4::key_of(um)));
+          if (q == 0) {
+            ca0 = ca;
+            cb0 = cb;
+          }
         }
         ca = __reduce_add_sync(0xFFFFFFFFu, ca);
         cb = __reduce_add_sync(0xFFFFFFFFu, cb);
+        ca0 = __reduce_add_sync(0xFFFFFFFFu, ca0);
+        cb0 = __reduce_add_sync(0xFFFFFFFFu, cb0);
         if (lane == 0) {
           atomicAdd(&st.spec_cnt[0], ca);
           atomicAdd(&st.spec_cnt[1], cb);
+          atomicAdd(&st.spec_cnt[3], ca0);
+          atomicAdd(&st.spec_cnt[4], cb0);
           st.est4[swarp] = umin;
         }
         Sel::sync();
         const uint32_t n8 = st.spec_cnt[0] & 0xFFFFu, n7 = st.spec_cnt[0] >> 16,
                        n6 = st.spec_cnt[1];
+        // the other sample units (not the first, where the candidates come
+        // from) must hold at least half of it: a first unit that holds the
+        // row's top (a sorted row) supports no speculation by itself
+        const uint32_t o8 = n8 - (st.spec_cnt[3] & 0xFFFFu), o7 = n7 - (st.spec_cnt[3] >> 16),
+                       o6 = n6 - st.spec_cnt[4];
+        const uint32_t half = (need + 1u) / 2u;
         uint32_t sk = 0u, nk = 0u;
-        if (n6 >= need) {
+        if (n6 >= need && (o6 >= half || n6 >= uint32_t(k))) {
           sk = s6;
           nk = n6;
-        } else if (n7 >= need) {
+        } else if (n7 >= need && (o7 >= half || n7 >= uint32_t(k))) {
           sk = s7;
           nk = n7;
-        } else if (n8 >= need) {
+        } else if (n8 >= need && (o8 >= half || n8 >= uint32_t(k))) {
           sk = s8;
           nk = n8;
         }
-        if (sk == 0u) {
+        if (sk == 0u && R == 1) {
           // Second round: the smallest of the 32 (warp, unit) maxima of the
           // sample, a lower candidate, counted the same way.
           uint32_t s2 = 0xFFFFFFFFu;
@@ -962,10 +998,14 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
           }
         }
         if (sk != 0u) {
-          // a candidate the sample alone shows k elements above is proven
-          if (nk >= uint32_t(k)) mk = sk;
-          else spec = (uint64_t(sk) << 32) - 1ull;
-          decided = true;
+          // A candidate the sample alone shows k elements above is proven:
+          // a floor for the bounds below (which may find a higher one).
+          if (nk >= uint32_t(k)) {
+            mk_floor = sk;
+          } else {
+            spec = (uint64_t(sk) << 32) - 1ull;
+            decided = true;
+          }
         }
       }
     }
@@ -1062,6 +1102,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
       }
     }
   }
+  mk = max(mk, mk_floor);
   if (stt == 0) {
     const uint64_t th0 = mk ? (uint64_t(mk) << 32) - 1ull : 0ull;
     if (th0) {
@@ -1252,7 +1293,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       }
       const int m_row = int((pc.L + kUnit - 1) / kUnit);
       const bool partial_tail = (pc.L % uint32_t(kUnit)) != 0;
-      const int wu = warm_units(p.k, nu);
+      const int wu = warm_units(p.k, nu, pc.L);
       for (int c0 = 0; c0 < nu; c0 += kPermChunk) {
         const int cs = min(nu - c0, kPermChunk);
         build_visit_order_warp(perm, cs, int64_t(pc.u_begin) + c0, pc.r, p.seed_lo, p.seed_hi,
@@ -1796,7 +1837,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               // it, so the producer can land the remaining units while the
               // warm start works on the first one: it starts once that one
               // is in.
-              const int wu = warm_units(k, pn.u_end - pn.u_begin);
+              const int wu = warm_units(k, pn.u_end - pn.u_begin, pn.L);
               const int need = warm_next == j ? 1 : wu;
               bool landed = true;
               for (int q = 0; q < need && landed; ++q) {

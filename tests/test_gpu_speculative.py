@@ -37,13 +37,13 @@ def _warp_slot(w: int, lane: int) -> int:
     return 4 * (32 * w + lane)
 
 
-def _plant_piece(x, row, u0, base_value, per_unit_after=2):
-    """Large scores in a piece whose first unit is u0: two per selector warp
-    share of unit u0, then `per_unit_after` in each of the next three units,
-    all above the first unit's."""
+def _plant_piece(x, row, u0, base_value, per_unit_after=2, per_warp=2):
+    """Large scores in a piece whose first unit is u0: `per_warp` per selector
+    warp share of unit u0, then `per_unit_after` in each of the next three
+    units, all above the first unit's."""
     for w in range(8):
-        for lane in range(2):
-            x[row, u0 * UNIT + _warp_slot(w, lane)] = base_value + 100 + 2 * w + lane
+        for lane in range(per_warp):
+            x[row, u0 * UNIT + _warp_slot(w, lane)] = base_value + 100 + per_warp * w + lane
     for q in range(1, 4):
         for j in range(per_unit_after):
             x[row, (u0 + q) * UNIT + 1000 + 37 * j] = base_value + 200 + 10 * q + j
@@ -97,6 +97,41 @@ def test_split_row_rescan(split):
     ov, oi = oracle_rows(y, k)
     assert_bit_exact(gv, gi, ov, oi, "after rescan")
     assert _status(ws) == 0
+
+
+@pytest.mark.parametrize("split", [1, 0])
+def test_k2048_row_rescan(split):
+    """k = 2048 on a 1M row (one piece, or eight): the speculative candidates
+    are the warps' 7th-largest-key bounds; eight planted scores per warp share
+    of each piece's first unit and fifty in each of the next three give the
+    sample 214 scores above them (the need is 160), the row fewer than 2048."""
+    from sparse_attention_indexer_row_gb300 import binding as B
+    rng = np.random.default_rng(14)
+    n, k = 128 * UNIT, 2048
+    x = (rng.standard_normal((1, n)).astype(np.float32) * 0.1 - 1).astype(np.float32)
+    starts = [0] if split == 1 else [16 * p for p in range(8)]
+    for piece, u0 in enumerate(starts):
+        _plant_piece(x, 0, u0, 1000.0 * piece, per_unit_after=50, per_warp=8)
+    gv, gi, ws = run_gpu(x, k, split=split, flags=B.TOPK_FLAG_IDENTITY_ORDER, return_ws=True)
+    ov, oi = oracle_rows(x, k)
+    assert_bit_exact(gv, gi, ov, oi, f"k2048 rescan (split={split})")
+    assert _status(ws) == B.TOPK_STATUS_RESCAN
+
+
+def test_k2048_iid_rows_start_speculatively():
+    """k = 2048 on i.i.d. 1M rows: far fewer admitted words than a proven
+    start gives (about 43,000 per row), and no rescan."""
+    from sparse_attention_indexer_row_gb300 import binding as B
+    rng = np.random.default_rng(15)
+    rows, n, k = 8, 1 << 20, 2048
+    x = rng.standard_normal((rows, n)).astype(np.float32)
+    gv, gi, ws = run_gpu(x, k, return_ws=True)
+    ov, oi = oracle_rows(x, k)
+    assert_bit_exact(gv, gi, ov, oi, "k2048 iid")
+    assert _status(ws) == 0
+    rc, surv, _, adm = B.topk_ws_stats(ws, rows, n, k, 0)
+    assert rc == 0 and min(surv) >= k
+    assert max(adm) < 8 * k, adm
 
 
 @pytest.mark.parametrize("rows,split", [(4, 0), (4, 1), (16, 0)])
