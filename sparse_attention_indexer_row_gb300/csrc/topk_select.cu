@@ -95,10 +95,11 @@ constexpr int kPermChunk = 256;              // units shuffled together (2M elem
 constexpr int kTrayMark = 2048;              // tray words that trigger the tray sort
 constexpr int kPruneStep = 512;              // new tray words that trigger a prune
 constexpr int kSelectSlack = 256;            // extra words a pruned tray may keep
-constexpr int kWarmUnits = 4;                // units a warm start reads (k <= 512)
+constexpr int kWarmUnits = 4;                // units a warm start reads (see warm_units)
 // (k <= 512 runs a five-stage ring: the producer can land all warm-start
-// units of a piece while the filters hold its first one)
-static_assert(kWarmUnits <= 5, "warm-start units fit in the ring");
+// units of a piece while the filters hold its first one; above, the four
+// warm-start units of a long row fill the four-stage ring)
+static_assert(kWarmUnits <= 4, "warm-start units fit in the smallest ring");
 // Speculative start: a piece with kWarmUnits warm-start units may start from a
 // threshold those units only make likely (about 3.6 k words of the row above
 // it).  It is taken when they hold at least 2.5 k * sample / row length
@@ -699,11 +700,6 @@ struct Top4 {
   }
   __device__ __forceinline__ uint32_t count_ge(uint32_t t) const {
     return (l0 >= t ? 1u : 0u) + (l1 >= t ? 1u : 0u) + (l2 >= t ? 1u : 0u) + (l3 >= t ? 1u : 0u);
-  }
-  __device__ __forceinline__ uint32_t bound(int m) const {
-    uint32_t T1, T2;
-    bound2(m, m, T1, T2);
-    return T1;
   }
   // Two searches at once (targets m1, m2), six trial keys per step, their
   // counts packed into two reductions.
