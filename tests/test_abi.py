@@ -72,3 +72,24 @@ def test_host_validation_returns_codes(B):
     assert B.topk_visit_order(0, 0, 0, 1, 4096) == B.TOPK_ERR_ARG
     assert B.topk_visit_order(257, 0, 0, 1, 4096) == B.TOPK_ERR_ARG
     assert B.topk_ws_status(0)[0] == B.TOPK_ERR_WS
+
+
+def test_pool_sizes_and_argument_codes(B):
+    """The block pool's workspace size and its host-side checks (no launch)."""
+    plain = B.topk_ws_bytes_ex(64, 1 << 20, 512, 0)
+    pool = B.topk_pool_ws_bytes(64, 1 << 20, 512, 2048, 64)
+    # the selection's own workspace plus one fp32 block maximum per 8 scores
+    assert pool >= plain + 64 * (1 << 17) * 4
+    assert B.topk_pool_ws_bytes(64, 1 << 20, 512, 2048 + 64, 64) == pool
+    for p, q in [(0, 0), (4, 5), (4, -1), (2100, 10)]:
+        assert B.topk_pool_ws_bytes(4, 1000, 8, p, q) == 0
+        assert B.topk_select_pool(4096, 4, 1000, 1000, None, 8, 4096, 4096, p, q, 4096, 4096) == \
+            B.TOPK_ERR_ARG
+    assert B.topk_pool_ws_bytes(4, 0, 8, 4, 1) == 0
+    assert B.topk_select_pool(0, 0, 1000, 1000, None, 8, 0, 0, 4, 1, 0, 0) == B.TOPK_OK
+    assert B.topk_select_pool(4096, 4, 1000, 999, None, 8, 4096, 4096, 4, 1, 4096, 4096) == \
+        B.TOPK_ERR_SHAPE
+    assert B.topk_select_pool(4096, 4, 1000, 1000, None, 8, 4096, 4096, 4, 1, None, 4096) == \
+        B.TOPK_ERR_NULL
+    assert B.topk_select_pool(4096, 4, 1000, 1000, None, 8, 4096, 4096, 4, 1, 4096, 4096 + 16) == \
+        B.TOPK_ERR_WS
