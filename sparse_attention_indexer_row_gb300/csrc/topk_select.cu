@@ -1440,6 +1440,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         return __float_as_uint(__ldg(row + e0 + pos));
       };
       if (__any_sync(0xFFFFFFFFu, gm != 0u)) {
+        // the inbox head as of now (it only grows: a safe bound for the room
+        // check below, read early so its latency overlaps the classification)
+        const uint32_t head_seen = *reinterpret_cast<volatile uint32_t*>(&st.head[par]);
         // A strict float compare is already the exact word test for every
         // value except NaN and values equal to the threshold's own (ties,
         // and -0.0 against +0.0): those few get the 64-bit word test.
@@ -1474,15 +1477,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         if (np) {
           uint32_t pos = atomicAdd(&st.tail[par], np);
           admitted += np;
-          // wait for room: the selectors free slots by advancing head
-          uint32_t it = timed_out ? kWaitLimit : 0u;
-          while (pos + np - *reinterpret_cast<volatile uint32_t*>(&st.head[par]) >
-                 uint32_t(kInbox)) {
-            if (++it > kWaitLimit) {
-              timed_out = true;
-              break;
+          // wait for room: the selectors free slots by advancing head (the
+          // head seen at the stage's start usually shows room already)
+          if (pos + np - head_seen > uint32_t(kInbox)) {
+            uint32_t it = timed_out ? kWaitLimit : 0u;
+            while (pos + np - *reinterpret_cast<volatile uint32_t*>(&st.head[par]) >
+                   uint32_t(kInbox)) {
+              if (++it > kWaitLimit) {
+                timed_out = true;
+                break;
+              }
+              __nanosleep(64);
             }
-            __nanosleep(64);
           }
           volatile uint64_t* ib = par ? inbox1 : inbox0;
           for (uint32_t mm = passm; mm; mm &= mm - 1u) {
