@@ -2106,7 +2106,9 @@ DeviceInfo g_devices[64];
 constexpr int kPoolSelThreads = 1024;
 constexpr uint32_t kPoolSeg = 32 * kPoolSelThreads;  // blocks per output segment (one word a thread)
 constexpr uint32_t kPoolCap = 8192;                  // keys the pool's fast path may collect
-constexpr int kPoolSmem = int(sizeof(uint32_t)) * (4096 + 2 * kPoolSelThreads + 2 * int(kPoolCap));
+constexpr uint32_t kPoolWide = 4096;                  // bitmap words of the one-pass write (131,072 blocks)
+constexpr int kPoolSmem =
+    int(sizeof(uint32_t)) * (4096 + 2 * kPoolSelThreads + 2 * int(kPoolCap) + int(kPoolWide));
 __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
     const float* bmax, int64_t bstride, const int32_t* lengths, int64_t n, int32_t pool_blocks,
     int32_t pinned, int32_t* out_pool);
@@ -2222,6 +2224,7 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
   uint32_t* eqbits = gtbits + kPoolSelThreads;
   uint32_t* lkey = eqbits + kPoolSelThreads;     // fast path: keys (the sample, then the list)
   uint32_t* lidx = lkey + kPoolCap;              // fast path: their block indices
+  uint32_t* wide_eq = lidx + kPoolCap;           // one-pass write: blocks equal to T (with hist: above)
   __shared__ uint32_t scratch[kPoolSelThreads / 32];
   __shared__ uint32_t s_bin, s_above, s_n;
   const int32_t r = blockIdx.x;
@@ -2256,6 +2259,14 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
       key[4 * q + 3] = to_key(v.w);
     }
   };
+  // histogram of keys in shared memory (key 0 = none)
+  auto feed_smem = [&](const uint32_t* keys, uint32_t cnt, uint32_t prefix, uint32_t pmask, int sh,
+                       uint32_t dmask) {
+    for (uint32_t i = t; i < cnt; i += kPoolSelThreads) {
+      const uint32_t k = keys[i];
+      if (k != 0u && (k & pmask) == prefix) atomicAdd(&hist[(k >> sh) & dmask], 1u);
+    }
+  };
   auto block_of = [&](uint32_t base, int q) -> uint32_t {  // load16's key q
     return base + 4u * kPoolSelThreads * uint32_t(q >> 2) + 4u * uint32_t(t) + uint32_t(q & 3);
   };
@@ -2265,15 +2276,14 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
   // match the prefix into hist.  want >= 1.  Returns the key of the want-th
   // largest (0 and all = true when every key is taken) and in need how many
   // keys equal to it are taken.
-  auto radix = [&](auto feed, uint32_t want, uint32_t& T, uint32_t& need, bool& all) {
+  auto radix = [&](auto feed, uint32_t want, uint32_t& T, uint32_t& need, bool& all,
+                   int passes = 3) {
     uint32_t prefix = 0, pmask = 0;
     need = want;
     all = false;
-    const int shifts[3] = {20, 8, 0};
-    const int widths[3] = {12, 12, 8};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int sh = shifts[pass];
-      const uint32_t dmask = (1u << widths[pass]) - 1u;
+    for (int pass = 0; pass < passes; ++pass) {
+      const int sh = pass == 0 ? 20 : (pass == 1 ? 8 : 0);  // digits of 12, 12 and 8 bits
+      const uint32_t dmask = pass < 2 ? 0xFFFu : 0xFFu;
       for (int j = t; j < 4096; j += kPoolSelThreads) hist[j] = 0u;
       __syncthreads();
       feed(prefix, pmask, sh, dmask);
@@ -2357,11 +2367,24 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
     if (ngroups * 8u <= kPoolCap) {
       // sample: keys [g * stride, g * stride + 8) of group g
       if (uint32_t(t) < ngroups) {
-        const uint32_t b0 = uint32_t(t) * stride;
+        const uint32_t b0 = uint32_t(t) * stride;  // a multiple of 128: 16-byte aligned
+        if (b0 + 8u <= nc) {
+          const float4 v0 = __ldg(reinterpret_cast<const float4*>(row + b0));
+          const float4 v1 = __ldg(reinterpret_cast<const float4*>(row + b0 + 4u));
+          lkey[8 * t + 0] = to_key(v0.x);
+          lkey[8 * t + 1] = to_key(v0.y);
+          lkey[8 * t + 2] = to_key(v0.z);
+          lkey[8 * t + 3] = to_key(v0.w);
+          lkey[8 * t + 4] = to_key(v1.x);
+          lkey[8 * t + 5] = to_key(v1.y);
+          lkey[8 * t + 6] = to_key(v1.z);
+          lkey[8 * t + 7] = to_key(v1.w);
+        } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t b = b0 + uint32_t(c);
-          lkey[8 * t + c] = b < nc ? to_key(row[b]) : 0u;
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t b = b0 + uint32_t(c);
+            lkey[8 * t + c] = b < nc ? to_key(row[b]) : 0u;
+          }
         }
       }
       __syncthreads();
@@ -2371,17 +2394,16 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
       uint32_t T0 = 0, e0 = 0;
       bool all0 = false;
       if (want64 <= scount) {
+        // (two passes: a 24-bit prefix is bound enough -- its bin's lower
+        // edge only lets a few more keys into the list)
         radix([&](uint32_t prefix, uint32_t pmask, int sh, uint32_t dmask) {
-                for (uint32_t i = t; i < scount; i += kPoolSelThreads) {
-                  const uint32_t k = lkey[i];
-                  if (k != 0u && (k & pmask) == prefix) atomicAdd(&hist[(k >> sh) & dmask], 1u);
-                }
-              }, uint32_t(want64), T0, e0, all0);
+                feed_smem(lkey, scount, prefix, pmask, sh, dmask);
+              }, uint32_t(want64), T0, e0, all0, 2);
       }
       // collect every key >= T0 (all keys when the sample cannot bound them)
       if (t == 0) s_n = 0u;
       __syncthreads();
-      const uint32_t lo = all0 || want64 > scount ? 1u : T0;
+      const uint32_t lo = all0 || want64 > scount ? 1u : max(T0, 1u);  // (0: no score)
       for (uint32_t base = 0; base < nc; base += kStep) {
         uint32_t key[16];
         load16(base, key);
@@ -2416,17 +2438,54 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
         uint32_t T, eq_take;
         bool all;
         radix([&](uint32_t prefix, uint32_t pmask, int sh, uint32_t dmask) {
-                for (uint32_t i = t; i < nl; i += kPoolSelThreads) {
-                  const uint32_t k = lkey[i];
-                  if ((k & pmask) == prefix) atomicAdd(&hist[(k >> sh) & dmask], 1u);
-                }
+                feed_smem(lkey, nl, prefix, pmask, sh, dmask);
               }, kb, T, eq_take, all);
-        sel = emit([&](uint32_t s0, uint32_t send) {
-                     for (uint32_t i = t; i < nl; i += kPoolSelThreads) {
-                       const uint32_t b = lidx[i];
-                       if (b >= s0 && b < send) set_bit(b, s0, lkey[i], T);
-                     }
-                   }, eq_take);
+        if (nc <= 32u * kPoolWide) {
+          // one pass: bitmaps of the whole row (hist: blocks above T, wide_eq:
+          // blocks equal to T), four words a thread, one packed prefix scan
+          uint32_t* gtw = hist;
+          for (uint32_t j = t; j < kPoolWide; j += kPoolSelThreads) {
+            gtw[j] = 0u;
+            wide_eq[j] = 0u;
+          }
+          __syncthreads();
+          for (uint32_t i = t; i < nl; i += kPoolSelThreads) {
+            const uint32_t b = lidx[i], key = lkey[i], bit = 1u << (b & 31u);
+            if (key > T) atomicOr(&gtw[b >> 5], bit);
+            else if (key == T) atomicOr(&wide_eq[b >> 5], bit);
+          }
+          __syncthreads();
+          constexpr int kW = int(kPoolWide) / kPoolSelThreads;  // words a thread
+          uint32_t gs = 0, es = 0;
+#pragma unroll
+          for (int q = 0; q < kW; ++q) {
+            gs += uint32_t(__popc(gtw[kW * t + q]));
+            es += uint32_t(__popc(wide_eq[kW * t + q]));
+          }
+          uint32_t tot;
+          const uint32_t before = pool_scan(gs | (es << 16), scratch, tot);
+          uint32_t gb = before & 0xFFFFu, eb = before >> 16;
+#pragma unroll
+          for (int q = 0; q < kW; ++q) {
+            const uint32_t w = uint32_t(kW * t + q);
+            const uint32_t g = gtw[w], e = wide_eq[w];
+            uint32_t esel = 0u, left = eq_take > eb ? eq_take - eb : 0u;
+            for (uint32_t m = e; m != 0u && left > 0u; m &= m - 1u, --left) esel |= m & (0u - m);
+            uint32_t pos = gb + min(eb, eq_take);
+            for (uint32_t m = g | esel; m != 0u; m &= m - 1u)
+              out[pos++] = int32_t(32u * w + uint32_t(__ffs(m) - 1));
+            gb += uint32_t(__popc(g));
+            eb += uint32_t(__popc(e));
+          }
+          sel = (tot & 0xFFFFu) + min(tot >> 16, eq_take);
+        } else {
+          sel = emit([&](uint32_t s0, uint32_t send) {
+                       for (uint32_t i = t; i < nl; i += kPoolSelThreads) {
+                         const uint32_t b = lidx[i];
+                         if (b >= s0 && b < send) set_bit(b, s0, lkey[i], T);
+                       }
+                     }, eq_take);
+        }
         done = true;
       }
     }
