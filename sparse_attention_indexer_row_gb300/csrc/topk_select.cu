@@ -95,12 +95,15 @@ constexpr int kPermChunk = 256;              // units shuffled together (2M elem
 constexpr int kTrayMark = 2048;              // tray words that trigger the tray sort
 constexpr int kPruneStep = 512;              // new tray words that trigger a prune
 constexpr int kSelectSlack = 256;            // extra words a pruned tray may keep
-constexpr int kWarmUnits = 4;                // units a warm start reads (see warm_units)
-// (k <= 512 runs a five-stage ring: the producer can land all warm-start
-// units of a piece while the filters hold its first one; above, the four
-// warm-start units of a long row fill the four-stage ring)
-static_assert(kWarmUnits <= 4, "warm-start units fit in the smallest ring");
-// Speculative start: a piece with kWarmUnits warm-start units may start from a
+constexpr int kWarmUnits = 4;                // units a warm start reads at most (see warm_units)
+constexpr int kWarmUnitsSmallK = 3;          // ... when each selector warp needs <= 64 (k <= 512)
+// (k <= 512 runs a five-stage ring: the producer lands the three warm-start
+// units of a piece while the filters hold its first one and keeps two more
+// copies in flight; above, the four warm-start units of a long row fill the
+// four-stage ring)
+static_assert(kWarmUnits <= 4 && kWarmUnitsSmallK <= kWarmUnits,
+              "warm-start units fit in the smallest ring");
+// Speculative start: a piece with a full warm-start sample may start from a
 // threshold those units only make likely (about 3.6 k words of the row above
 // it).  It is taken when they hold at least 2.5 k * sample / row length
 // elements at or above it, at most kSpecMaxNeed (so: long rows).
@@ -767,13 +770,19 @@ __host__ __device__ inline uint64_t spec_need(int k, int wu, uint32_t L) {
   return (5ull * uint64_t(k) * sample + 2ull * L - 1ull) / (2ull * L);
 }
 
-// Units a piece's warm start reads: kWarmUnits (at most the piece's units)
-// when each warp needs at most 64 elements (k <= 512); above that, four units
-// only where a speculative start may be taken (a long row), else one.
+// The full warm-start sample of a piece, in units: kWarmUnitsSmallK when each
+// selector warp needs at most 64 elements (k <= 512), else kWarmUnits.
+__host__ __device__ inline int warm_cap(int k) {
+  return (k + kNS - 1) / kNS <= 64 ? kWarmUnitsSmallK : kWarmUnits;
+}
+
+// Units a piece's warm start reads: warm_cap (at most the piece's units) for
+// k <= 512; above that, kWarmUnits only where a speculative start may be
+// taken (a long row), else one.
 __host__ __device__ inline int warm_units(int k, int nu, uint32_t L) {
-  const int m = (k + kNS - 1) / kNS;
-  const int w = nu < 1 ? 1 : (nu < kWarmUnits ? nu : kWarmUnits);
-  if (m <= 64) return w;
+  const int cap = warm_cap(k);
+  const int w = nu < 1 ? 1 : (nu < cap ? nu : cap);
+  if ((k + kNS - 1) / kNS <= 64) return w;
   return (w == kWarmUnits && L > 0u && spec_need(k, w, L) <= kSpecMaxNeed) ? w : 1;
 }
 
@@ -822,7 +831,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
   // never counts NaN, and misses only -0.0 against a +0.0 bound).  Only when
   // no candidate is supported do the lane lists below run.
   const int nu = pw.u_end - pw.u_begin;
-  if (wu == kWarmUnits && nu >= kWarmUnits) {
+  if (wu == warm_cap(k) && nu >= wu) {
     const uint64_t need64 = spec_need(k, wu, pw.L);
     if (need64 <= kSpecMaxNeed) {
       const uint32_t need = uint32_t(need64);
@@ -951,7 +960,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
           nk = n8;
         }
         if (sk == 0u && R == 1) {
-          // Second round: the smallest of the 32 (warp, unit) maxima of the
+          // Second round: the smallest of the 8 wu (warp, unit) maxima of the
           // sample, a lower candidate, counted the same way.
           uint32_t s2 = 0xFFFFFFFFu;
 #pragma unroll

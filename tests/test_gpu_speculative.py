@@ -1,7 +1,7 @@
 """GPU parity of the speculative start and its rescan.
 
-A long piece may start from a threshold that its first four 8192-element
-units only make likely.  These inputs are built so that, with units visited in
+A long piece may start from a threshold that its first 8192-element units
+(three for k <= 512, four above) only make likely.  These inputs are built so that, with units visited in
 address order, every piece's sample promises more large scores than the row
 holds: the start misses, the row must be selected again from global memory,
 and the result must still equal the oracle bit for bit (with the status word's
@@ -40,7 +40,8 @@ def _warp_slot(w: int, lane: int) -> int:
 def _plant_piece(x, row, u0, base_value, per_unit_after=2, per_warp=2):
     """Large scores in a piece whose first unit is u0: `per_warp` per selector
     warp share of unit u0, then `per_unit_after` in each of the next three
-    units, all above the first unit's."""
+    units, all above the first unit's (a sample of three units sees the
+    first two of those)."""
     for w in range(8):
         for lane in range(per_warp):
             x[row, u0 * UNIT + _warp_slot(w, lane)] = base_value + 100 + per_warp * w + lane
@@ -58,8 +59,9 @@ def _status(ws):
 
 @pytest.mark.parametrize("quantised", [False, True])
 def test_unsplit_row_rescan(quantised):
-    """One row of 16 units (one piece, no split), k = 64: the sample holds
-    53 scores above the speculative bound, the row only 53 < 64."""
+    """One row of 16 units (one piece, no split), k = 64: the three sample
+    units hold 39 scores at or above the speculative bound (the need is 30),
+    the row only 53 < 64."""
     from sparse_attention_indexer_row_gb300 import binding as B
     rng = np.random.default_rng(11)
     n, k = 16 * UNIT, 64
