@@ -51,6 +51,19 @@ def _dist():
     return world, rank, local
 
 
+def _launches_per_call(rows: int, n: int, has_lengths: bool, pool: bool) -> int:
+    """Kernels one call launches: the selection kernel; before it, for a
+    batch of at least 152 rows with per-row lengths and rows of at most 4096
+    units of 8192 elements, the kernel that orders the shared queue by row
+    length; after it, with a block pool, the pool kernel."""
+    per = 1
+    if has_lengths and rows >= 152 and -(-n // 8192) <= 4096:
+        per += 1
+    if pool:
+        per += 1
+    return per
+
+
 def _workload(name: str) -> synth.Workload:
     return synth.make(name)
 
@@ -313,7 +326,7 @@ def run_gb300(args, world, rank, local):
             "path": "pinned host -> device copy, " + ("topk_select_pool" if pool else "topk_select") +
                     " (C ABI), device -> pinned host",
         },
-        "gpu_launches": args.steps * (2 if pool else 1),
+        "gpu_launches": args.steps * _launches_per_call(rows, n, w.lengths is not None, bool(pool)),
         "clocks": clocks.summary(),
         "survivors": {
             "mean_per_row": round(float(np.mean(surv)), 1), "max_per_row": int(max(surv)),
