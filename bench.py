@@ -363,10 +363,20 @@ def cpu_baseline(w: synth.Workload, cpu_seconds: float, rows_per_pass=None):
         if t_total * min(cores, sample.shape[0]) >= cpu_seconds or passes >= 50:
             break
     rows_done = passes * sample.shape[0]
+    # the same oracle on one thread, over the first few rows of the sample
+    few = min(4, sample.shape[0])
+    t = time.perf_counter()
+    _, _, st = orc.topk(sample[:few], w.k, lengths=None if lens is None else lens[:few], n=w.n,
+                        nthreads=1)
+    t_one = time.perf_counter() - t
+    if st != 0:
+        raise RuntimeError(f"oracle status {st}")
     return {"value": round(rows_done / t_total, 2), "unit": UNIT,
             "cores": min(cores, sample.shape[0]), "kind": "oracle",
             "sample": f"{passes} pass(es) over {sample.shape[0]} rows of {w.name} "
-                      f"({t_total:.2f} s wall)"}
+                      f"({t_total:.2f} s wall)",
+            "single_thread": {"value": round(few / t_one, 2), "unit": UNIT, "cores": 1,
+                              "sample": f"the first {few} rows of the batch, once"}}
 
 
 def run_reference(args, world, rank):

@@ -66,3 +66,14 @@ def test_bench_rejects_fewer_than_three_warmup_steps():
          "--steps", "1", "--warmup", "2"],
         cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert out.returncode != 0 and "warmup" in out.stderr
+
+
+def test_cpu_baseline_leg_reports_all_cores_and_one_thread():
+    import bench
+    from sparse_attention_indexer_row_gb300 import synth
+    w = synth.make("c1")
+    cb = bench.cpu_baseline(w, 0.2)
+    assert cb["kind"] == "oracle" and cb["unit"] == bench.UNIT
+    assert cb["value"] > 0 and 1 <= cb["cores"] <= w.rows and w.name in cb["sample"]
+    one = cb["single_thread"]
+    assert one["value"] > 0 and one["cores"] == 1 and one["unit"] == bench.UNIT
