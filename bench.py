@@ -7,7 +7,12 @@ Normal(0,1) scores with k = 512, the decode shape the throughput metric is
 quoted on.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--pool P,Q] [--timeline]
+
+``--gpus N`` must match the number of ranks: N = 1 runs in this process, N > 1
+runs under torchrun (one rank per GPU).  ``--timeline`` also records one launch
+with the instrumented build of the library (per-CTA stamps; see
+``sparse_attention_indexer_row_gb300/timeline.py``) and adds its summary.
 
 Under torchrun each rank runs the same per-GPU batch on its own GPU (weak
 scaling, no collective on the data path); the timed region is bracketed by a
@@ -53,13 +58,14 @@ def _dist():
     return world, rank, local
 
 
-def _launches_per_call(rows: int, n: int, has_lengths: bool, pool: bool) -> int:
+def _launches_per_call(rows: int, n: int, has_lengths: bool, pool: bool, plan_sms: int) -> int:
     """Kernels one call launches: the selection kernel; before it, for a
-    batch of at least 152 rows with per-row lengths and rows of at most 4096
-    units of 8192 elements, the kernel that orders the shared queue by row
-    length; after it, with a block pool, the pool kernel."""
+    batch of at least as many rows as the plan has CTAs (the device's SM
+    count, at most 256) with per-row lengths and rows of at most 4096 units of
+    8192 elements, the kernel that orders the shared queue by row length;
+    after it, with a block pool, the pool kernel."""
     per = 1
-    if has_lengths and rows >= 152 and -(-n // 8192) <= 4096:
+    if has_lengths and rows >= plan_sms and -(-n // 8192) <= 4096:
         per += 1
     if pool:
         per += 1
@@ -224,10 +230,27 @@ def run_gb300(args, world, rank, local):
             t1.record(stream)
         torch.cuda.synchronize()
         barrier()
-    local_ms = sum(a.elapsed_time(b) for a, b in pairs) if flush else t0.elapsed_time(t1)
+    per_launch = [a.elapsed_time(b) for a, b in pairs]
+    local_ms = sum(per_launch) if flush else t0.elapsed_time(t1)
     total_ms = D.max_over_ranks(local_ms, device=dev)
     ms_per_step = total_ms / args.steps
     value = world * rows / (ms_per_step / 1e3)
+    launch_stats = None
+    if flush:
+        # the same launches back to back on one buffer, no flush: L2-resident
+        # scores after the first (a latency figure beside the HBM one)
+        h0 = torch.cuda.Event(enable_timing=True)
+        h1 = torch.cuda.Event(enable_timing=True)
+        select(bufs[0])
+        h0.record(stream)
+        for _ in range(args.steps):
+            select(bufs[0])
+        h1.record(stream)
+        torch.cuda.synchronize()
+        q = np.percentile(per_launch, [10, 50, 90])
+        launch_stats = {"flushed_ms": {"p10": round(float(q[0]), 5), "median": round(float(q[1]), 5),
+                                       "p90": round(float(q[2]), 5), "launches": len(per_launch)},
+                        "hot_l2_ms": round(h0.elapsed_time(h1) / args.steps, 5)}
 
     # End to end through the same C call: pinned host scores in, results out.
     host_pin = host.pin_memory()
@@ -344,7 +367,9 @@ def run_gb300(args, world, rank, local):
             "path": "pinned host -> device copy, " + ("topk_select_pool" if pool else "topk_select") +
                     " (C ABI), device -> pinned host",
         },
-        "gpu_launches": args.steps * _launches_per_call(rows, n, w.lengths is not None, bool(pool)),
+        "gpu_launches": args.steps * _launches_per_call(
+            rows, n, w.lengths is not None, bool(pool),
+            min(256, torch.cuda.get_device_properties(dev).multi_processor_count)),
         "clocks": clocks.summary(),
         "survivors": {
             "mean_per_row": round(float(np.mean(surv)), 1), "max_per_row": int(max(surv)),
@@ -357,9 +382,40 @@ def run_gb300(args, world, rank, local):
         "torch_topk": None if tk_ms is None else {
             "ms": round(tk_ms, 4), "gbs": round(alg_bytes / (tk_ms / 1e3) / 1e9, 1)},
     }
+    if launch_stats:
+        line["launch_ms"] = launch_stats
+    if args.timeline:
+        line["timeline"] = timeline_of(B, bufs[0], w, lengths, vals, idx, ws, stream, pool,
+                                       out_pool if pool else None, line["clocks"].get("sm_mhz"))
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
+
+
+def timeline_of(B, x, w, lengths, vals, idx, ws, stream, pool, out_pool, sm_mhz):
+    """One launch of the same call through the instrumented build, summarised
+    per CTA (stamps in µs after the earliest CTA start; cycles at the clock the
+    timed region saw)."""
+    from sparse_attention_indexer_row_gb300 import timeline as TLM
+    lib = TLM.load()
+    P, S = B._ptr, B._stream
+
+    def call(l):
+        if pool:
+            rc = l.topk_select_pool(P(x), w.rows, w.n, w.row_stride, P(lengths), w.k, P(vals),
+                                    P(idx), pool[0], pool[1], P(out_pool), P(ws), S(stream))
+        else:
+            rc = l.topk_select(P(x), w.rows, w.n, w.row_stride, P(lengths), w.k, P(vals), P(idx),
+                               P(ws), S(stream))
+        if rc != 0:
+            raise RuntimeError(f"instrumented selection returned {rc}")
+
+    for _ in range(3):
+        call(lib)
+    table = TLM.record(lib, call, stream)
+    out = TLM.summarize(table, float(sm_mhz or 2070.0))
+    out["build"] = "libtopk_gb300_timeline.so (-DTOPK_TIMELINE=1), one launch after three"
+    return out
 
 
 def cpu_baseline(w: synth.Workload, cpu_seconds: float, rows_per_pass=None):
@@ -453,11 +509,17 @@ def main():
                          "(topk_select_pool; e.g. 2048,64)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--timeline", action="store_true",
+                    help="also record one launch with the instrumented build and summarise it")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
     world, rank, local = _dist()
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but {world} rank(s): for N > 1 launch one rank per GPU "
+                 "with torchrun (python -m torch.distributed.run --nproc-per-node N bench.py "
+                 "--gpus N ...)")
     if world > 1:
         import torch.distributed as dist
         if args.impl == "reference":

@@ -62,17 +62,31 @@ extern "C" {
  * read by topk_ws_status). */
 #define TOPK_STATUS_NAN 1u        /* a NaN inside some row's valid prefix */
 #define TOPK_STATUS_BAD_LENGTH 2u /* lengths[r] outside [0, n]; clamped */
-#define TOPK_STATUS_TIMEOUT 4u    /* a bounded wait on a bulk copy gave up; the
-                                     affected rows' outputs are unspecified */
+#define TOPK_STATUS_TIMEOUT 4u    /* a bounded wait (for a bulk copy, or for a
+                                     hand-over between the CTA's warps) gave up;
+                                     the affected rows' outputs are unspecified */
 #define TOPK_STATUS_RESCAN 8u     /* information only: some row's speculative
                                      starting threshold left fewer than k of its
                                      scores above it, and the row was selected
                                      again from global memory (results exact) */
+#define TOPK_STATUS_BOUNDS 16u    /* set by the debug build only (compiled with
+                                     -DTOPK_DEBUG_BOUNDS=1): a shared- or
+                                     global-memory index failed its check and
+                                     the write was skipped */
 
 /* Flags for topk_select_ex. */
 #define TOPK_FLAG_IDENTITY_ORDER 1u /* visit units in address order instead of
                                        the shuffled order (diagnostic: the
                                        result is the same, the speed is not) */
+#define TOPK_FLAG_TEST_STALL 256u   /* test of the bounded waits only: in every
+                                       CTA the copy producer stops for good in
+                                       front of its fourth ring stage, and every
+                                       wait of the call gives up after 16,384
+                                       polls (about a millisecond).  The call
+                                       finishes, sets TOPK_STATUS_TIMEOUT and
+                                       leaves the outputs unspecified; with
+                                       split = 1 the workspace stays reusable
+                                       (each row is one piece, no ticket) */
 
 /* Largest supported k. */
 #define TOPK_MAX_K 2048
@@ -87,7 +101,8 @@ extern "C" {
  * The workspace holds a status word, per-row survivor and sort counters, the
  * per-row tickets of the split-row leader election and, when rows are split,
  * the CTAs' partial top-k lists (8 bytes x k rounded up to a power of two, per
- * CTA).  It is a pure function of (rows, n, k).
+ * CTA).  It is a pure function of (rows, n, k): it covers the plan of any
+ * device with up to 256 SMs, so a workspace sized once serves every GPU.
  */
 size_t topk_ws_bytes(int32_t rows, int64_t n, int32_t k);
 
@@ -125,7 +140,9 @@ int topk_select(const float* scores, int32_t rows, int64_t n,
 
 /*
  * topk_split_plan -- the number of CTAs the automatic plan gives each row
- * (1 = unsplit).  A pure function of (rows, n); 0 for an invalid shape.
+ * (1 = unsplit) on the current device: the plan runs one CTA per SM (at most
+ * 256), so it depends on (rows, n) and the device's SM count; with no device
+ * to query it plans for 152 SMs (GB300).  0 for an invalid shape.
  */
 int32_t topk_split_plan(int32_t rows, int64_t n);
 
@@ -190,32 +207,48 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
 int topk_visit_order(int32_t m, int32_t row, int64_t first_unit,
                      uint64_t seed, int32_t* order_out, void* stream);
 
+/*
+ * topk_timeline_read -- diagnostic of the instrumented build only (the library
+ * compiled with -DTOPK_TIMELINE=1; every other build returns TOPK_ERR_ARG and
+ * touches nothing).  Synchronises `stream`, copies the selection kernel's
+ * timeline table to host_out (TOPK_TIMELINE_CTAS x TOPK_TIMELINE_SLOTS
+ * uint64 values, CTA-major) and clears it.  Per CTA: global-timer stamps (ns)
+ * of its start, set-up, first and last copy, each role's exit and four events
+ * of each of its first eight pieces, its SM id and piece count, and SM cycles
+ * spent per activity by one thread of each role.  Slot meanings are listed
+ * with the table in topk_select.cu; the table holds the calls since the last
+ * read (a CTA's stamps: the latest call).
+ */
+#define TOPK_TIMELINE_CTAS 512
+#define TOPK_TIMELINE_SLOTS 64
+int topk_timeline_read(unsigned long long* host_out, void* stream);
 
 /*
  * topk_select_noalloc -- topk_select for callers that cannot allocate device
  * memory.  (An addition of this library: the pages describe no such call.)
  *
- * Some callers cannot call cudaMalloc where they select: code that runs while
- * a stream is being captured into a CUDA graph and must not allocate, real-time
- * paths that forbid allocation, or plug-ins whose host framework owns all
- * device memory and hands them only input and output buffers.  This entry
+ * Some callers cannot call cudaMalloc where they select: real-time paths that
+ * forbid allocation once they run (an allocation can block on the driver and
+ * synchronise the device), and plug-ins whose host framework owns all device
+ * memory and hands them only their input and output buffers.  This entry
  * point needs no workspace argument: it uses a 16 MiB array compiled into the
  * library (a file-scope __device__ array), which every GPU that loads the
- * library keeps until the process exits.  It calls no cudaMalloc or cudaFree.
+ * library holds until the process exits.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
  *
  *   Arguments as topk_select, without `ws`.  `status_or_null`: optional device
  *   uint32 that receives this call's status word (TOPK_STATUS_* bits).
  *
  *   Limit: shapes whose topk_ws_bytes(rows, n, k) exceeds 16 MiB return
- *   TOPK_ERR_NOSPACE (for example, k = 2048 on fewer than 152 rows needs about
- *   8.4 MiB; one CTA per row needs about 20 bytes per row).
+ *   TOPK_ERR_NOSPACE and enqueue nothing.
  *
- *   The first call on a device looks up the array's device address (with that
- *   device current); make that first call before capturing a stream into a
- *   graph.  Every call shares the one array: the call clears the parts that
- *   must start at zero (status, tickets, counters) on `stream`, and two calls
- *   that may overlap on the GPU -- on different streams, or from different
- *   host threads -- race on it and must be serialised by the caller.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *   first call before any stream capture.  Every call shares the one array:
+ *   each call clears, on `stream`, the parts that must start at zero (status,
+ *   tickets, counters, per-row words), and two calls that may overlap on the
+ *   GPU -- on different streams, or from different host threads -- race on it
+ *   and must be serialised by the caller.
  *
  * Returns TOPK_OK, TOPK_ERR_SHAPE, TOPK_ERR_NULL, TOPK_ERR_NOSPACE or
  * TOPK_ERR_LAUNCH.

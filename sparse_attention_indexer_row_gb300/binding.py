@@ -25,8 +25,12 @@ TOPK_STATUS_NAN = 1
 TOPK_STATUS_BAD_LENGTH = 2
 TOPK_STATUS_TIMEOUT = 4
 TOPK_STATUS_RESCAN = 8
+TOPK_STATUS_BOUNDS = 16
 TOPK_POOL_BLOCK = 8
 TOPK_FLAG_IDENTITY_ORDER = 1
+TOPK_FLAG_TEST_STALL = 256
+TOPK_TIMELINE_CTAS = 512
+TOPK_TIMELINE_SLOTS = 64
 TOPK_MAX_K = 2048
 
 # Every symbol the header exports, with (restype, argtypes).
@@ -42,6 +46,7 @@ SIGNATURES = {
     "topk_ws_status": (ctypes.c_int, [_P, ctypes.POINTER(_U32), _P]),
     "topk_ws_stats": (ctypes.c_int, [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P]),
     "topk_visit_order": (ctypes.c_int, [_I32, _I32, _I64, _U64, _P, _P]),
+    "topk_timeline_read": (ctypes.c_int, [_P, _P]),
     "topk_select_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _P, _P, _P, _P]),
     "topk_pool_ws_bytes": (_SZ, [_I32, _I64, _I32, _I32, _I32]),
     "topk_select_pool": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _P, _P, _I32, _I32,
@@ -49,12 +54,14 @@ SIGNATURES = {
 }
 
 
-def _load() -> ctypes.CDLL:
-    if not _LIB_PATH.exists():
+def load_library(path: Path = _LIB_PATH) -> ctypes.CDLL:
+    """Load one build of the library (the product one by default, or an
+    instrumented variant) with every exported signature declared."""
+    if not path.exists():
         raise ImportError(
-            f"{_LIB_PATH.name} is not built; run __graft_entry__.build() "
+            f"{path.name} is not built; run __graft_entry__.build() "
             "(nvcc for sm_103a) first -- there is no CPU fallback")
-    lib = ctypes.CDLL(str(_LIB_PATH))
+    lib = ctypes.CDLL(str(path))
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res
@@ -62,7 +69,7 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-LIB = _load()
+LIB = load_library()
 
 
 def _ptr(x):

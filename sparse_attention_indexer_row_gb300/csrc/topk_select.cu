@@ -116,15 +116,134 @@ constexpr int kPreFinal = 8;
 constexpr int kPreFinalMin = 16;
 constexpr int kMaxSplit = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;    // polls before a wait gives up
+// With TOPK_FLAG_TEST_STALL: every wait gives up after this many polls, and
+// the producer stops for good in front of ring stage kTestStallStage (its
+// barrier never completes), so that the waits behind it run out.
+constexpr uint32_t kTestWaitLimit = 1u << 14;
+constexpr int kTestStallStage = 3;
 
-// Launch plan, tuned for GB300's 152 SMs (results never depend on it).
-constexpr int kSms = 152;
+// Launch plan: one CTA per SM of the device, at most kMaxFlatCtas (results
+// never depend on it).  A batch of at least as many rows as that count is not
+// split.  Workspace sizes are computed for kMaxFlatCtas, the largest count a
+// plan can use, so that they stay a function of the shape alone.
+constexpr int kSmsDefault = 152;   // GB300's count: the plan when no device can be queried
 constexpr int kMaxFlatCtas = 256;  // persistent grid cap (workspace slots)
 constexpr int kMinFlatUnits = 16;  // a row is split into shares of at least 512 KB
 constexpr int kMinSegUnits = 4;    // at least 128 KB per split segment
-constexpr int kManyRows = kSms;    // rows per call from which rows are not split
 
 constexpr uint64_t kDefaultSeed = 0x5EEDC0DE1234ABCDull;
+
+// ---------------------------------------------------------------------------
+// Timeline (an instrumented build only: compiled with -DTOPK_TIMELINE=1).
+// Each CTA of the selection kernel stamps the global timer at the events
+// below and accumulates SM cycles per activity of one thread of each role
+// (producer lane 0, filter warp 0 lane 0, selector thread 0) into its row of
+// g_timeline; topk_timeline_read copies the table out.  In the normal build
+// every TL_* macro is empty and the table does not exist.
+#ifndef TOPK_TIMELINE
+#define TOPK_TIMELINE 0
+#endif
+constexpr int kTlSlots = 64;   // u64 slots per CTA
+constexpr int kTlPieces = 8;   // pieces recorded per CTA
+enum TlSlot : int {
+  kTlStart = 0,       // kernel entry
+  kTlSetup = 1,       // after the set-up barrier
+  kTlFirstCopy = 2,   // producer: first copy issued
+  kTlLastCopy = 3,    // producer: last copy issued
+  kTlProdExit = 4,    // producer: done
+  kTlFiltFirst = 5,   // filter warp 0: first stage taken (threshold in hand)
+  kTlFiltExit = 6,    // filter warp 0: done
+  kTlSelExit = 7,     // selectors: done
+  kTlInfo = 8,        // SM id | pieces << 32
+  kTlPiece0 = 10,     // per piece p: 4 slots from kTlPiece0 + 4p:
+                      //   +0 starting threshold published, +1 filter warp 0
+                      //   takes its first stage, +2 filter warp 0 releases its
+                      //   last stage, +3 selectors done with it (row written
+                      //   or partial list published; a leader after its merge)
+  kTlCyc0 = 48,       // cycle accumulators, see TlCyc
+};
+enum TlCyc : int {
+  kCycFiltWaitFull = 0,  // filter warp 0: waiting for a stage to land
+  kCycFiltWaitTheta,     // filter warp 0: waiting for a piece's starting threshold
+  kCycFiltCand,          // filter warp 0: candidate path (classify, reserve, write)
+  kCycFiltStages,        // filter warp 0: stages taken (a count)
+  kCycFiltCandStages,    // filter warp 0: stages that took the candidate path (a count)
+  kCycSelWarm,           // selectors: warm starts
+  kCycSelTake,           // selectors: moving inbox words to the tray
+  kCycSelPrune,          // selectors: prunes (select without sort)
+  kCycSelSort,           // selectors: tray sorts and merges before a piece's end
+  kCycSelEnd,            // selectors: piece ends (final sort, output or ticket, leader merge)
+  kCycSelPoll,           // selectors: polling for work
+  kCycSelLeader,         // selectors: leader merges (a count)
+  kCycProdWaitEmpty,     // producer: waiting for a free ring stage
+  kCycSelRescan,         // selectors: rescans (a count)
+  kCycCount
+};
+static_assert(kTlPiece0 + 4 * kTlPieces <= kTlCyc0 && kTlCyc0 + kCycCount <= kTlSlots,
+              "timeline slots");
+
+#if TOPK_TIMELINE
+constexpr int kTlCtas = 512;   // CTAs recorded
+
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ unsigned long long tl_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ unsigned long long g_timeline[kTlCtas * kTlSlots];
+#define TL_SET(slot, v)                                                                  \
+  do {                                                                                   \
+    if (blockIdx.x < unsigned(kTlCtas)) g_timeline[blockIdx.x * kTlSlots + (slot)] = (v); \
+  } while (0)
+#define TL_PIECE(pc, off)                                   \
+  do {                                                      \
+    if ((pc) >= 0 && (pc) < kTlPieces) TL_SET(kTlPiece0 + 4 * (pc) + (off), tl_now()); \
+  } while (0)
+#define TL_CYC_DECL(name) unsigned long long name[kCycCount] = {}
+#define TL_CLK(var) const long long var = clock64()
+#define TL_ACC(arr, which, since) ((arr)[which] += (unsigned long long)(clock64() - (since)))
+#define TL_CNT(arr, which) (++(arr)[which])
+#define TL_FLUSH(arr)                                                   \
+  do {                                                                  \
+    for (int q_ = 0; q_ < kCycCount; ++q_)                              \
+      if ((arr)[q_]) TL_SET(kTlCyc0 + q_, (arr)[q_]);                   \
+  } while (0)
+#else
+#define TL_SET(slot, v) ((void)0)
+#define TL_PIECE(pc, off) ((void)0)
+#define TL_CYC_DECL(name) [[maybe_unused]] int name = 0
+#define TL_CLK(var) ((void)0)
+#define TL_ACC(arr, which, since) ((void)(arr))
+#define TL_CNT(arr, which) ((void)(arr))
+#define TL_FLUSH(arr) ((void)(arr))
+#endif
+
+// ---------------------------------------------------------------------------
+// Bounds checks (the debug build only: compiled with -DTOPK_DEBUG_BOUNDS=1).
+// IN_BOUNDS(cond, status) guards each shared- or global-memory write whose
+// index is computed at run time (tray, kept list, leader-merge area, partial
+// lists, outputs, block maxima, pool output): when cond is false the debug
+// build sets TOPK_STATUS_BOUNDS and skips the write.  In the normal build it
+// is the constant true.
+#ifndef TOPK_DEBUG_BOUNDS
+#define TOPK_DEBUG_BOUNDS 0
+#endif
+#if TOPK_DEBUG_BOUNDS
+__device__ __forceinline__ bool bounds_ok(bool ok, uint32_t* status) {
+  if (!ok) atomicOr(status, TOPK_STATUS_BOUNDS);
+  return ok;
+}
+#define IN_BOUNDS(cond, status) bounds_ok((cond), (status))
+#else
+#define IN_BOUNDS(cond, status) true
+#endif
 
 // The CTA: filter warps, selector warps and one producer warp.
 constexpr int kNF = 8;
@@ -195,10 +314,12 @@ bool shape_ok(int32_t rows, int64_t n, int32_t k) {
   return rows >= 0 && n >= 1 && n <= INT32_MAX && k >= 1 && k <= TOPK_MAX_K;
 }
 
-int32_t auto_split(int32_t rows, int64_t n) {
-  if (rows <= 0 || rows >= kManyRows) return 1;
+// CTAs per row of the automatic plan for `plan_sms` CTAs (the device's SM
+// count, at most kMaxFlatCtas).
+int32_t auto_split(int32_t rows, int64_t n, int plan_sms) {
+  if (rows <= 0 || rows >= plan_sms) return 1;
   const int64_t m = (n + kUnit - 1) / kUnit;
-  int64_t s = kSms / rows;
+  int64_t s = plan_sms / rows;
   const int64_t by_len = m / kMinSegUnits;
   if (s > by_len) s = by_len;
   if (s > kMaxSplit) s = kMaxSplit;
@@ -208,9 +329,9 @@ int32_t auto_split(int32_t rows, int64_t n) {
 
 // Partial-list slots a call may need.  With the automatic plan a short batch
 // may run either plan (the choice depends on whether lengths are passed).
-size_t partial_slots(int32_t rows, int32_t split_arg, int32_t split) {
+size_t partial_slots(int32_t rows, int32_t split_arg, int32_t split, int plan_sms) {
   size_t slots = split > 1 ? size_t(rows) * size_t(split) : 0;
-  if (split_arg == 0 && rows > 0 && rows < kManyRows) {
+  if (split_arg == 0 && rows > 0 && rows < plan_sms) {
     const size_t flat = 2 * size_t(kMaxFlatCtas);
     if (flat > slots) slots = flat;
   }
@@ -274,6 +395,9 @@ struct Params {
   const int32_t* order;  // queue plan: rows, longest first (null: index order)
   float* bmax;        // block pool: block maxima per row (null: not asked for)
   int64_t bstride;    // block pool: row stride of bmax, in blocks
+  int64_t nslots;       // partial-list slots in the workspace
+  uint32_t wait_limit;  // polls before a wait gives up
+  int32_t stall_at;     // test only: ring stage the producer stops in front of (-1: none)
 };
 
 // What the producer tells the filters about a stage.
@@ -356,6 +480,7 @@ struct CtaState {
   int first_issued;                // pieces whose first stage the producer has issued
   uint32_t fprog;                  // stages filter warp 0 has released
   int sel_pre;                     // selector step: pre-final due
+  uint32_t wait_limit;             // polls before a wait gives up (the kernel's parameter)
   unsigned long long theta[2];     // threshold word of the piece using inbox p
   Piece table[kTable];             // piece descriptors, by sequence number
 };
@@ -598,6 +723,7 @@ __device__ __forceinline__ void write_row(const Params& p, int32_t r, const uint
   int32_t* oi = p.out_idx + int64_t(r) * p.k;
   for (int j = t; j < p.k; j += nt) {
     const uint64_t w = kept[j];
+    if (!IN_BOUNDS(r >= 0 && r < p.rows, p.status)) break;
     if (w == 0ull) {
       ov[j] = -__int_as_float(0x7F800000);
       oi[j] = -1;
@@ -799,6 +925,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
                                               unsigned long long* row_spec, CtaState& st,
                                               int w, const float* ring, const StageDesc* desc,
                                               uint64_t* full, int nstage, int k, int stt) {
+#define wl (*reinterpret_cast<volatile uint32_t*>(&st.wait_limit))
   using Sel = Team<kNST, 1>;
   const int lane = stt & 31, swarp = stt >> 5;
   const int m_warm = (k + kNS - 1) / kNS;
@@ -811,7 +938,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
     const uint32_t g = pw.g_first + uint32_t(q);
     const int slot = int(g % uint32_t(nstage));
     // every reader observes the copy's completion itself (already complete)
-    if (!mbar_wait(&full[slot], (g / uint32_t(nstage)) & 1u, kWaitLimit)) ok = false;
+    if (!mbar_wait(&full[slot], (g / uint32_t(nstage)) & 1u, wl)) ok = false;
     d = desc[slot];
     src = ring + slot * kUnit;
     copied = waligned ? (d.nvalid & ~3u) : 0u;
@@ -1126,9 +1253,11 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
     }
     __threadfence_block();
     *reinterpret_cast<volatile int*>(&st.warm_pub) = w + 1;
+    TL_PIECE(w, 0);
   }
   Sel::sync();  // the bounds are read before the next warm start rewrites them
   return ok;
+#undef wl
 }
 
 // The layer-20 block pool's block maxima, computed in the same pass (The
@@ -1138,7 +1267,10 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
 // out; NaN only when every valid score is NaN), +0.0 above -0.0.  Lanes with
 // an even thread index store one float per block of the stage.
 __device__ __forceinline__ void store_block_max(const float (&x)[kEPT], uint32_t valid, int ft,
-                                                uint32_t e0, uint32_t nvalid, float* brow) {
+                                                uint32_t e0, uint32_t nvalid, float* brow,
+                                                int64_t bstride, uint32_t* status) {
+  (void)bstride;
+  (void)status;
   float bm[kF4];
   if (valid == 0xFFFFFFFFu) {  // a full unit: no element to leave out
 #pragma unroll
@@ -1177,7 +1309,9 @@ __device__ __forceinline__ void store_block_max(const float (&x)[kEPT], uint32_t
     float* dst = brow + ((e0 + 4u * uint32_t(ft)) >> 3);
 #pragma unroll
     for (int u = 0; u < kF4; ++u)
-      if (uint32_t(4 * (ft + kNFT * u)) < nvalid) dst[(kNFT / 2) * u] = bm[u];
+      if (uint32_t(4 * (ft + kNFT * u)) < nvalid &&
+          IN_BOUNDS(int64_t((e0 + 4u * uint32_t(ft)) >> 3) + (kNFT / 2) * u < bstride, status))
+        dst[(kNFT / 2) * u] = bm[u];
   }
 }
 
@@ -1205,6 +1339,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int kp = p.kp, k = p.k;
+  // (the wait limit is read from shared memory where it is used: a register
+  // held across every role would cost the selector loop a spill)
+#define wl (*reinterpret_cast<volatile uint32_t*>(&st.wait_limit))
+  if (tid == 0) TL_SET(kTlStart, tl_now());
 
   for (int j = tid; j < kp; j += kThreads) kept[j] = 0ull;
   for (int j = tid; j < kInbox; j += kThreads) {
@@ -1226,6 +1364,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     st.first_issued = 0;
     st.fprog = 0u;
     st.flags = 0;
+    st.wait_limit = p.wait_limit;
     for (int i = 0; i < nstage; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kNF);
@@ -1233,6 +1372,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     mbar_init_fence();
   }
   __syncthreads();
+  if (tid == 0) TL_SET(kTlSetup, tl_now());
 
   // ---------------- producer: the plan, a2 visiting orders, a3 copies ----------------
   if (warp == kProducerWarp) {
@@ -1240,15 +1380,19 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     // scores are read once: their lines go first when L2 needs room
     const uint64_t l2pol = l2_policy_evict_first();
     bool gave_up = false;
+    bool stalled = false;  // test only: the producer stopped for good
+    TL_CYC_DECL(tlc);
     uint32_t g = 0;  // stages issued (lane 0)
     int stage = 0;
     uint32_t phase = 0;
     int seq = 0;
     // wait for ring slot `stage` to be free, then hand it a descriptor
     auto next_slot = [&]() {
+      TL_CLK(c0);
       if (g >= uint32_t(nstage) &&
-          !mbar_wait_sleep(&empty[stage], phase ^ 1u, gave_up ? 1u : kWaitLimit, 64))
+          !mbar_wait_sleep(&empty[stage], phase ^ 1u, gave_up ? 1u : wl, 64))
         gave_up = true;
+      TL_ACC(tlc, kCycProdWaitEmpty, c0);
     };
     auto advance = [&]() {
       ++g;
@@ -1266,9 +1410,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (got == 2) continue;
       if (lane == 0) {
         // the descriptor slot is free once the selectors finished piece seq - kTable
-        uint32_t it = gave_up ? kWaitLimit : 0u;
+        uint32_t it = gave_up ? wl : 0u;
         while (*reinterpret_cast<volatile int*>(&st.sel_pieces) < seq - kTable + 1) {
-          if (++it > kWaitLimit) {
+          if (++it > wl) {
             gave_up = true;
             break;
           }
@@ -1317,6 +1461,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             }
           }
           for (int i = 0; i < cs; ++i) {
+            if (int64_t(g) == int64_t(p.stall_at)) {
+              // test only: stop in front of this stage for good (its full
+              // barrier never completes, so the waits behind it run out)
+              stalled = true;
+              break;
+            }
             next_slot();
             const uint32_t u = uint32_t(pc.u_begin + c0) + (perm[i] & uint32_t(kPermChunk - 1));
             const uint32_t e0 = u * uint32_t(kUnit);
@@ -1336,6 +1486,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             } else {
               mbar_arrive(&full[stage]);
             }
+            if (g == 0u) TL_SET(kTlFirstCopy, tl_now());
             // Until a piece's first wu stages are issued, their ring slots'
             // barriers may still be in an earlier phase: the selectors look at
             // them only after this count says the stages are on their way.
@@ -1344,16 +1495,21 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           }
         }
         __syncwarp();  // the order buffer is reused by the next chunk
+        stalled = __shfl_sync(0xFFFFFFFFu, stalled, 0);
+        if (stalled) break;
       }
       ++seq;
+      if (stalled) break;
     }
     if (lane == 0) {
+      TL_SET(kTlLastCopy, tl_now());
       *reinterpret_cast<volatile int*>(&st.npieces) = seq;
       // the copies of the last stages have landed before this warp (and so
       // the CTA) can leave, even if the filters gave up on them
       for (uint32_t q = g > uint32_t(nstage) ? g - uint32_t(nstage) : 0u; q < g; ++q)
-        if (!mbar_wait(&full[q % uint32_t(nstage)], (q / uint32_t(nstage)) & 1u, kWaitLimit))
+        if (!mbar_wait(&full[q % uint32_t(nstage)], (q / uint32_t(nstage)) & 1u, wl))
           gave_up = true;
+      if (stalled) return;  // (test only: no end marker either)
       next_slot();
       StageDesc d;
       d.e0 = 0;
@@ -1363,6 +1519,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       desc[stage] = d;
       mbar_arrive(&full[stage]);
       if (gave_up) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
+      TL_FLUSH(tlc);
+      TL_SET(kTlInfo, (unsigned long long)smid() | ((unsigned long long)seq << 32));
+      TL_SET(kTlProdExit, tl_now());
     }
     return;
   }
@@ -1379,12 +1538,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     uint32_t phase = 0;
     int par = 0;
     int32_t r = 0;
+    const bool tl0 = tid == 0;  // (timeline: filter warp 0, lane 0)
+    TL_CYC_DECL(tlc);
+    [[maybe_unused]] int tl_piece = -1;
+    (void)tl0;
     const float* row = p.scores;
     bool aligned = true;
     // every exit decision is warp-uniform: a wait that gave up in any lane
     // ends the warp's loop
     for (;;) {
-      if (!mbar_wait_sleep(&full[stage], phase, kWaitLimit, 32)) timed_out = true;
+      TL_CLK(cw);
+      if (!mbar_wait_sleep(&full[stage], phase, wl, 32)) timed_out = true;
+      if (tl0) TL_ACC(tlc, kCycFiltWaitFull, cw);
       const StageDesc d = desc[stage];
       if (__any_sync(0xFFFFFFFFu, timed_out)) {
         timed_out = true;
@@ -1397,10 +1562,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         // The selectors set the piece's starting threshold once this unit
         // has landed, and only after piece seq - 2 (which used the same
         // inbox, counters and threshold word) is finished.
+        TL_CLK(ct);
         if (lane == 0) {
           uint32_t it = 0;
           while (*reinterpret_cast<volatile int*>(&st.warm_pub) < seq + 1) {
-            if (++it > kWaitLimit) {
+            if (++it > wl) {
               timed_out = true;
               break;
             }
@@ -1410,6 +1576,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         if (__any_sync(0xFFFFFFFFu, timed_out)) {
           timed_out = true;
           break;
+        }
+        if (tl0) {
+          TL_ACC(tlc, kCycFiltWaitTheta, ct);
+          if (seq == 0) TL_SET(kTlFiltFirst, tl_now());
+          tl_piece = seq;
+          TL_PIECE(seq, 1);
         }
         r = int32_t(d.r);
         row = p.scores + int64_t(r) * p.row_stride;
@@ -1428,7 +1600,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       const uint32_t copied = aligned ? (nvalid & ~3u) : 0u;
       float x[kEPT];
       const uint32_t valid = load_share(x, src, row, e0, nvalid, copied, ft);  // bit e: in the row
-      if (p.bmax != nullptr) store_block_max(x, valid, ft, e0, nvalid, p.bmax + int64_t(r) * p.bstride);
+      if (p.bmax != nullptr)
+        store_block_max(x, valid, ft, e0, nvalid, p.bmax + int64_t(r) * p.bstride, p.bstride,
+                        p.status);
       // Most stages have no element past the threshold: the test first folds
       // each float4 group into one bit (a superset: it also passes NaN, ties
       // and padding); only flagged groups are re-read (where they sit: the
@@ -1448,7 +1622,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         if (pos < copied) return __float_as_uint(src[pos]);
         return __float_as_uint(__ldg(row + e0 + pos));
       };
+      if (tl0) TL_CNT(tlc, kCycFiltStages);
+      TL_CLK(cc);
       if (__any_sync(0xFFFFFFFFu, gm != 0u)) {
+        if (tl0) TL_CNT(tlc, kCycFiltCandStages);
         // the inbox head as of now (it only grows: a safe bound for the room
         // check below, read early so its latency overlaps the classification)
         const uint32_t head_seen = *reinterpret_cast<volatile uint32_t*>(&st.head[par]);
@@ -1489,10 +1666,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           // wait for room: the selectors free slots by advancing head (the
           // head seen at the stage's start usually shows room already)
           if (pos + np - head_seen > uint32_t(kInbox)) {
-            uint32_t it = timed_out ? kWaitLimit : 0u;
+            uint32_t it = timed_out ? wl : 0u;
             while (pos + np - *reinterpret_cast<volatile uint32_t*>(&st.head[par]) >
                    uint32_t(kInbox)) {
-              if (++it > kWaitLimit) {
+              if (++it > wl) {
                 timed_out = true;
                 break;
               }
@@ -1507,11 +1684,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           }
         }
       }
+      if (tl0) TL_ACC(tlc, kCycFiltCand, cc);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[stage]);
         if (warp == 0) *reinterpret_cast<volatile uint32_t*>(&st.fprog) = ++released;
       }
+      if (tl0 && (d.tag & kLast)) TL_PIECE(tl_piece, 2);
       if (d.tag & kLast) {
         __syncwarp();
         admitted = __reduce_add_sync(0xFFFFFFFFu, admitted);
@@ -1533,6 +1712,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (saw_nan) atomicOr(p.status, TOPK_STATUS_NAN);
       if (timed_out) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
     }
+    if (tl0) {
+      TL_FLUSH(tlc);
+      TL_SET(kTlFiltExit, tl_now());
+    }
     return;
   }
 
@@ -1550,6 +1733,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   uint32_t head = 0, head_other = 0;  // inbox heads: this piece's parity, the other one
   int par = 0;
   int warm_next = 0;  // next piece whose starting threshold is to be set
+  TL_CYC_DECL(tlc);   // (timeline: accumulated by selector thread 0)
 
   // Publish a threshold to the filters (and to the row's other CTAs).
   // Every word passed here is proven: at least k words of the row are at or
@@ -1656,7 +1840,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           int at = 0;
           if (lane == 0) at = atomicAdd(&st.cnt2, __popc(mask));
           at = __shfl_sync(0xFFFFFFFFu, at, 0);
-          if (keep[u]) tray[at + __popc(mask & lt_mask)] = w[u];
+          if (keep[u] && IN_BOUNDS(at + __popc(mask & lt_mask) < kTray, p.status))
+            tray[at + __popc(mask & lt_mask)] = w[u];
         }
       }
     }
@@ -1672,6 +1857,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     // to a power of two, at least one word per selector thread) and merge
     // them in
     const int P = max(next_pow2_dev(max(r, 1)), kNST);
+    if (!IN_BOUNDS(P <= kTray, p.status)) return;
     for (int t = r + stt; t < P; t += kNST) tray[t] = 0ull;
     Sel::sync();
     team_sort_desc<Sel>(tray, P, 2, stt);
@@ -1698,9 +1884,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     for (int j = stt; j < n; j += kNST) {
       volatile uint64_t* slot = ib + ((h + uint32_t(j)) & (kInbox - 1));
       uint64_t w = *slot;
-      uint32_t it = timed_out ? kWaitLimit : 0u;
+      uint32_t it = timed_out ? wl : 0u;
       while (w == 0ull) {
-        if (++it > kWaitLimit) {
+        if (++it > wl) {
           timed_out = true;
           break;
         }
@@ -1708,7 +1894,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         w = *slot;
       }
       *slot = 0ull;
-      tray[tray_n + j] = w;
+      if (IN_BOUNDS(tray_n + j < kTray, p.status)) tray[tray_n + j] = w;
     }
     __threadfence_block();  // the emptied slots are visible before head moves
     Sel::sync();
@@ -1755,7 +1941,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           int at = 0;
           if (lane == 0) at = atomicAdd(&st.cnt2, __popc(mask));
           at = __shfl_sync(0xFFFFFFFFu, at, 0);
-          if (keep) tray[tray_n + at + __popc(mask & lt_mask)] = w;
+          if (keep && IN_BOUNDS(tray_n + at + __popc(mask & lt_mask) < kTray, p.status))
+            tray[tray_n + at + __popc(mask & lt_mask)] = w;
         }
       }
       Sel::sync();
@@ -1768,7 +1955,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   for (int j = 0;; ++j) {
     // the producer publishes piece j's descriptor before its first stage
     if (stt == 0) {
-      uint32_t it = timed_out ? kWaitLimit : 0u;
+      uint32_t it = timed_out ? wl : 0u;
       int have = 0;
       for (;;) {
         if (*reinterpret_cast<volatile int*>(&st.pieces_pub) > j) {
@@ -1779,7 +1966,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           have = *reinterpret_cast<volatile int*>(&st.pieces_pub) > j ? 1 : 0;
           break;
         }
-        if (++it > kWaitLimit) {
+        if (++it > wl) {
           timed_out = true;
           break;
         }
@@ -1807,8 +1994,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       // One lane polls until there is a batch to take or the piece is done;
       // the rest of the team waits at the barrier.  The finished-filter count
       // is read before the tail, so a full count means the tail is final.
+      TL_CLK(cpoll);
       if (stt == 0) {
-        uint32_t it = timed_out ? kWaitLimit : 0u;
+        uint32_t it = timed_out ? wl : 0u;
         int n = 0, done = 0, warm = 0, pre = 0;
         for (;;) {
           // First: a piece (this one or the next) still waiting for its
@@ -1837,6 +2025,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               }
               __threadfence_block();
               *reinterpret_cast<volatile int*>(&st.warm_pub) = warm_next + 1;
+              TL_PIECE(warm_next, 0);
               warm = 2;
               break;
             }
@@ -1886,7 +2075,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             break;
           }
           if (n > 0 || done) break;
-          if (++it > kWaitLimit) {
+          if (++it > wl) {
             timed_out = true;
             done = 1;
             break;
@@ -1906,27 +2095,43 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       const uint64_t sth = *reinterpret_cast<volatile unsigned long long*>(&st.theta[par]);
       if (sth > theta) theta = sth;
       Sel::sync();
+      if (stt == 0) TL_ACC(tlc, kCycSelPoll, cpoll);
       if (warm) {
+        TL_CLK(cw);
         if (warm == 1 && !warm_start_piece(p.scores, p.row_stride, p.row_theta, p.row_spec, st,
                                            warm_next, ring, desc, full, nstage, k, stt))
           timed_out = true;
+        if (stt == 0) TL_ACC(tlc, kCycSelWarm, cw);
         ++warm_next;
         continue;
       }
       if (pre) {
         pre_done = true;
+        TL_CLK(ct);
         if (n > 0) take(n);
+        if (stt == 0) TL_ACC(tlc, kCycSelTake, ct);
+        TL_CLK(cs);
         if (tray_n > 0) process_tray(true, true, pc);
+        if (stt == 0) TL_ACC(tlc, kCycSelSort, cs);
         continue;
       }
       if (done) break;
+      TL_CLK(ct);
       take(n);
-      if (tray_n >= kTrayMark) process_tray(true, false, pc);
-      else if (tray_n >= pruned + kPruneStep) process_tray(false, false, pc);
+      if (stt == 0) TL_ACC(tlc, kCycSelTake, ct);
+      TL_CLK(cs);
+      if (tray_n >= kTrayMark) {
+        process_tray(true, false, pc);
+        if (stt == 0) TL_ACC(tlc, kCycSelSort, cs);
+      } else if (tray_n >= pruned + kPruneStep) {
+        process_tray(false, false, pc);
+        if (stt == 0) TL_ACC(tlc, kCycSelPrune, cs);
+      }
     }
 
     // end of the piece: final sort, then the row's output (directly, or
     // through the split-row ticket)
+    TL_CLK(cend);
     if (tray_n > 0) {
       if (kept_n > 0 && tray_n <= kNST && kp >= kNST) {
         // Only the last stages' words are left (the kept list holds the best
@@ -1964,7 +2169,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     } else {
       // a7: publish the local list, take a ticket; the last ticket merges.
       uint64_t* mine = p.partials + int64_t(pc.slot) * kp;
-      for (int q = stt; q < kp; q += kNST) mine[q] = kept[q];
+      if (IN_BOUNDS(pc.slot >= 0 && pc.slot < p.nslots, p.status))
+        for (int q = stt; q < kp; q += kNST) mine[q] = kept[q];
       __threadfence();
       Sel::sync();
       if (stt == 0) {
@@ -1973,6 +2179,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       }
       Sel::sync();
       if (st.leader) {
+        if (stt == 0) TL_CNT(tlc, kCycSelLeader);
         __threadfence();
         // (read now, used after the merge: the row's pieces all published
         // their speculative words before their tickets)
@@ -1999,6 +2206,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               const int64_t go = pc.first_cta + o;
               slot = 2 * go + (flat_lo(go, M, G) / p.u_full == pc.r ? 0 : 1);
             }
+            if (!IN_BOUNDS(slot >= 0 && slot < p.nslots, p.status)) slot = 0;
             st.gsrc[stt] = p.partials + slot * kp;
           }
           Sel::sync();
@@ -2014,7 +2222,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               const int t = b + u * kNST;
-              if (t < total) slots[kp + t] = v[u];
+              if (t < total && IN_BOUNDS(kp + t < kInbox + kTray, p.status)) slots[kp + t] = v[u];
             }
           }
           gathered += takeq;
@@ -2065,6 +2273,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       // (as a lone piece: the row's shared words are already reset)
       Piece lone = pc;
       lone.contributors = 1;
+      if (stt == 0) TL_CNT(tlc, kCycSelRescan);
       rescan(lone, redo_lb);
       if (stt == 0) {
         atomicAdd(&p.sorts[pc.r], nsorts);
@@ -2088,10 +2297,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       st.spec[par] = 0ull;
       __threadfence_block();
       *reinterpret_cast<volatile int*>(&st.sel_pieces) = j + 1;
+      TL_ACC(tlc, kCycSelEnd, cend);
+      TL_PIECE(j, 3);
     }
   }
   timed_out = Sel::sync_or(timed_out);
   if (stt == 0 && timed_out) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
+  if (stt == 0) {
+    TL_FLUSH(tlc);
+    TL_SET(kTlSelExit, tl_now());
+  }
+#undef wl
 }
 
 __global__ void __launch_bounds__(32)
@@ -2120,7 +2336,7 @@ constexpr int kPoolSmem =
     int(sizeof(uint32_t)) * (4096 + 2 * kPoolSelThreads + 2 * int(kPoolCap) + int(kPoolWide));
 __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
     const float* bmax, int64_t bstride, const int32_t* lengths, int64_t n, int32_t pool_blocks,
-    int32_t pinned, int32_t* out_pool);
+    int32_t pinned, int32_t* out_pool, uint32_t* status);
 
 cudaError_t configure_device(int* sms) {
   int dev = 0;
@@ -2149,8 +2365,37 @@ cudaError_t configure_device(int* sms) {
   return cudaSuccess;
 }
 
-int32_t resolve_split(int32_t rows, int64_t n, int32_t split) {
-  return split == 0 ? auto_split(rows, n) : split;
+int32_t resolve_split(int32_t rows, int64_t n, int32_t split, int plan_sms) {
+  return split == 0 ? auto_split(rows, n, plan_sms) : split;
+}
+
+// Partial-list slots a workspace is sized for: enough for any plan count up
+// to kMaxFlatCtas (auto_split and the flat plan only grow with the count).
+size_t sized_slots(int32_t rows, int64_t n, int32_t split) {
+  return partial_slots(rows, split, resolve_split(rows, n, split, kMaxFlatCtas), kMaxFlatCtas);
+}
+
+// The planning count of the current device: its SM count, at most
+// kMaxFlatCtas; kSmsDefault when no device can be queried.
+int device_plan_sms() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return kSmsDefault;
+  }
+  int v = cached[dev].load();
+  if (v == 0) {
+    int count = 0;
+    if (cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        count < 1) {
+      cudaGetLastError();
+      return kSmsDefault;
+    }
+    v = count < kMaxFlatCtas ? count : kMaxFlatCtas;
+    cached[dev].store(v);
+  }
+  return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -2226,7 +2471,8 @@ __device__ __forceinline__ uint32_t pool_scan(uint32_t v, uint32_t* scratch, uin
 // (three passes and a marking pass).
 __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
     const float* bmax, int64_t bstride, const int32_t* lengths, int64_t n, int32_t pool_blocks,
-    int32_t pinned, int32_t* out_pool) {
+    int32_t pinned, int32_t* out_pool, uint32_t* status) {
+  (void)status;
   extern __shared__ __align__(16) uint32_t psm[];
   uint32_t* hist = psm;                          // 4096 bins
   uint32_t* gtbits = psm + 4096;                 // output bitmaps, one word a thread
@@ -2352,8 +2598,9 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
       uint32_t esel = 0u, left = eq_take > eb ? eq_take - eb : 0u;
       for (uint32_t m = e; m != 0u && left > 0u; m &= m - 1u, --left) esel |= m & (0u - m);
       uint32_t pos = gb + min(eb, eq_take);
-      for (uint32_t m = g | esel; m != 0u; m &= m - 1u)
-        out[pos++] = int32_t(s0 + 32u * uint32_t(t) + uint32_t(__ffs(m) - 1));
+      for (uint32_t m = g | esel; m != 0u; m &= m - 1u, ++pos)
+        if (IN_BOUNDS(pos < uint32_t(pool_blocks), status))
+          out[pos] = int32_t(s0 + 32u * uint32_t(t) + uint32_t(__ffs(m) - 1));
       gt_run += tot & 0xFFFFu;
       eq_run += tot >> 16;
       __syncthreads();
@@ -2481,8 +2728,9 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
             uint32_t esel = 0u, left = eq_take > eb ? eq_take - eb : 0u;
             for (uint32_t m = e; m != 0u && left > 0u; m &= m - 1u, --left) esel |= m & (0u - m);
             uint32_t pos = gb + min(eb, eq_take);
-            for (uint32_t m = g | esel; m != 0u; m &= m - 1u)
-              out[pos++] = int32_t(32u * w + uint32_t(__ffs(m) - 1));
+            for (uint32_t m = g | esel; m != 0u; m &= m - 1u, ++pos)
+              if (IN_BOUNDS(pos < uint32_t(pool_blocks), status))
+                out[pos] = int32_t(32u * w + uint32_t(__ffs(m) - 1));
             gb += uint32_t(__popc(g));
             eb += uint32_t(__popc(e));
           }
@@ -2579,14 +2827,15 @@ using namespace topk;
 // ---------------------------------------------------------------------------
 // Workspace for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc at the point where they select: code
-// running inside a CUDA-graph capture that must not allocate, allocation-free
-// real-time paths, plug-ins whose host framework owns every allocation and
-// hands out only input and output buffers.  For them topk_select_noalloc uses
-// this file-scope device array as its workspace.  Every GPU that loads this
-// library keeps the array (kNoAllocWsBytes) until the process exits.  In host
-// code `g_noalloc_ws` names a host-side stand-in, not device memory: its
-// device address is looked up once per device with cudaGetSymbolAddress.
+// Some callers cannot call cudaMalloc at the point where they select:
+// real-time paths that forbid allocation once running (an allocation can
+// block on the driver), and plug-ins whose host framework owns every
+// allocation and hands out only input and output buffers.  For them
+// topk_select_noalloc uses this file-scope device array as its workspace.
+// Every GPU that loads this library keeps the array (kNoAllocWsBytes) until
+// the process exits.  In host code `g_noalloc_ws` names a host-side stand-in,
+// not device memory: its device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current.
 constexpr size_t kNoAllocWsBytes = size_t(16) << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocWsBytes];
 
@@ -2635,7 +2884,7 @@ int topk_select_noalloc(const float* scores, int32_t rows, int64_t n, int64_t ro
   // The array keeps the previous call's contents: the status word, tickets,
   // counters and row thresholds (everything before the partial lists) must
   // start at zero.
-  const WsLayout wl = ws_layout(rows, next_pow2(k), partial_slots(rows, 0, resolve_split(rows, n, 0)));
+  const WsLayout wl = ws_layout(rows, next_pow2(k), sized_slots(rows, n, 0));
   if (cudaMemsetAsync(ws, 0, wl.partials, st) != cudaSuccess) return TOPK_ERR_LAUNCH;
   const int rc = topk_select(scores, rows, n, row_stride, lengths_or_null, k, out_vals, out_idx,
                              ws, stream);
@@ -2653,13 +2902,12 @@ extern "C" {
 
 int32_t topk_split_plan(int32_t rows, int64_t n) {
   if (!shape_ok(rows, n, 1)) return 0;
-  return auto_split(rows, n);
+  return auto_split(rows, n, device_plan_sms());
 }
 
 size_t topk_ws_bytes_ex(int32_t rows, int64_t n, int32_t k, int32_t split) {
   if (!shape_ok(rows, n, k) || split < 0 || split > kMaxSplit) return 0;
-  const int32_t S = resolve_split(rows, n, split);
-  return ws_layout(rows, next_pow2(k), partial_slots(rows, split, S)).total;
+  return ws_layout(rows, next_pow2(k), sized_slots(rows, n, split)).total;
 }
 
 size_t topk_ws_bytes(int32_t rows, int64_t n, int32_t k) {
@@ -2678,13 +2926,15 @@ static int launch_select(const float* scores, int32_t rows, int64_t n, int64_t r
   if (!scores || !out_vals || !out_idx) return TOPK_ERR_NULL;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TOPK_ERR_WS;
 
-  const int32_t S = resolve_split(rows, n, split);
-  const int32_t kp = next_pow2(k);
-  const WsLayout wl = ws_layout(rows, kp, partial_slots(rows, split, S));
-  const int64_t u_full = (n + kUnit - 1) / kUnit;
-
-  int sms = kSms;
+  int sms = kSmsDefault;
   if (configure_device(&sms) != cudaSuccess) return TOPK_ERR_LAUNCH;
+  const int plan_sms = sms < kMaxFlatCtas ? sms : kMaxFlatCtas;
+  const int32_t S = resolve_split(rows, n, split, plan_sms);
+  const int32_t kp = next_pow2(k);
+  // (the partial lists come last: the other offsets do not depend on the
+  // slot count, which is at most the sized one)
+  const WsLayout wl = ws_layout(rows, kp, sized_slots(rows, n, split));
+  const int64_t u_full = (n + kUnit - 1) / kUnit;
 
   unsigned char* w = static_cast<unsigned char*>(ws);
   Params p;
@@ -2711,13 +2961,17 @@ static int launch_select(const float* scores, int32_t rows, int64_t n, int64_t r
   p.row_theta = reinterpret_cast<unsigned long long*>(w + wl.theta);
   p.row_spec = reinterpret_cast<unsigned long long*>(w + wl.spec);
   p.partials = reinterpret_cast<uint64_t*>(w + wl.partials);
+  p.nslots = int64_t(partial_slots(rows, split, S, plan_sms));
   p.seed_lo = uint32_t(seed);
   p.seed_hi = uint32_t(seed >> 32);
   p.flags = flags;
+  const bool stall = (flags & TOPK_FLAG_TEST_STALL) != 0;
+  p.wait_limit = stall ? kTestWaitLimit : kWaitLimit;
+  p.stall_at = stall ? kTestStallStage : -1;
 
-  const int64_t cap = sms < kMaxFlatCtas ? sms : kMaxFlatCtas;
+  const int64_t cap = plan_sms;
   int64_t G;
-  const bool flat = split == 0 && lengths_or_null == nullptr && rows < kManyRows;
+  const bool flat = split == 0 && lengths_or_null == nullptr && rows < plan_sms;
   if (flat) {
     // one CTA per SM, equal shares of the batch's units: at least one CTA
     // per row, and rows split only into shares of kMinFlatUnits or more
@@ -2735,7 +2989,7 @@ static int launch_select(const float* scores, int32_t rows, int64_t n, int64_t r
     // first (a CTA that drew short rows takes more of them)
     const int64_t items = int64_t(rows) * S;
     G = items < cap ? items : cap;
-    p.plan = rows >= kManyRows ? kPlanQueue : kPlanItems;
+    p.plan = rows >= plan_sms ? kPlanQueue : kPlanItems;
   }
   if (G < 1) G = 1;
   p.queue = reinterpret_cast<uint32_t*>(w + wl.queue);
@@ -2790,8 +3044,9 @@ int topk_select_pool(const float* scores, int32_t rows, int64_t n, int64_t row_s
                          stream, 0, kDefaultSeed, 0u, bmax, pl.bstride);
   if (rc != TOPK_OK) return rc;
   // the best blocks among each row's blocks that are not pinned, and the pool
-  pool_select_kernel<<<rows, kPoolSelThreads, kPoolSmem, st>>>(bmax, pl.bstride, lengths_or_null, n,
-                                                        pool_blocks, pinned_blocks, out_pool);
+  pool_select_kernel<<<rows, kPoolSelThreads, kPoolSmem, st>>>(
+      bmax, pl.bstride, lengths_or_null, n, pool_blocks, pinned_blocks, out_pool,
+      reinterpret_cast<uint32_t*>(w));
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
 }
 
@@ -2811,8 +3066,7 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
                   void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return TOPK_ERR_WS;
   if (!shape_ok(rows, n, k) || split < 0 || split > kMaxSplit) return TOPK_ERR_SHAPE;
-  const int32_t S = resolve_split(rows, n, split);
-  const WsLayout wl = ws_layout(rows, next_pow2(k), partial_slots(rows, split, S));
+  const WsLayout wl = ws_layout(rows, next_pow2(k), sized_slots(rows, n, split));
   unsigned char* w = static_cast<unsigned char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return TOPK_ERR_LAUNCH;
@@ -2826,6 +3080,27 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
     if (cudaMemset(w + offs[i], 0, bytes) != cudaSuccess) return TOPK_ERR_LAUNCH;
   }
   return TOPK_OK;
+}
+
+int topk_timeline_read(unsigned long long* host_out, void* stream) {
+#if TOPK_TIMELINE
+  static_assert(kTlCtas == TOPK_TIMELINE_CTAS && kTlSlots == TOPK_TIMELINE_SLOTS,
+                "timeline table shape");
+  if (!host_out) return TOPK_ERR_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TOPK_ERR_LAUNCH;
+  void* dev = nullptr;
+  if (cudaGetSymbolAddress(&dev, g_timeline) != cudaSuccess) return TOPK_ERR_LAUNCH;
+  const size_t bytes = sizeof(unsigned long long) * size_t(kTlCtas) * size_t(kTlSlots);
+  if (cudaMemcpy(host_out, dev, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TOPK_ERR_LAUNCH;
+  if (cudaMemset(dev, 0, bytes) != cudaSuccess) return TOPK_ERR_LAUNCH;
+  return TOPK_OK;
+#else
+  (void)host_out;
+  (void)stream;
+  return TOPK_ERR_ARG;
+#endif
 }
 
 int topk_visit_order(int32_t m, int32_t row, int64_t first_unit, uint64_t seed,

@@ -18,8 +18,10 @@ def host_threads() -> int:
 
 
 def run_gpu(scores: np.ndarray, k: int, lengths=None, n=None, split=0, seed=None, flags=0,
-            device="cuda", ws=None, check_canaries=True, return_ws=False):
-    """Select on the GPU through the C ABI; outputs sit between canary zones."""
+            device="cuda", ws=None, check_canaries=True, return_ws=False, lib=None):
+    """Select on the GPU through the C ABI; outputs sit between canary zones.
+    `lib`: another build of the library (a ctypes handle from
+    binding.load_library), else the product one."""
     import torch
 
     from sparse_attention_indexer_row_gb300 import binding as B
@@ -36,9 +38,15 @@ def run_gpu(scores: np.ndarray, k: int, lengths=None, n=None, split=0, seed=None
         assert nbytes > 0
         ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
     kw = {} if seed is None else {"seed": seed}
-    rc = B.topk_select_ex(x, rows, n, stride, lt, k, vbuf[CANARY:].data_ptr() if total else
-                          vbuf, ibuf[CANARY:].data_ptr() if total else ibuf, ws, None, split,
-                          flags=flags, **kw)
+    vptr = vbuf[CANARY:].data_ptr() if total else vbuf.data_ptr()
+    iptr = ibuf[CANARY:].data_ptr() if total else ibuf.data_ptr()
+    if lib is None:
+        rc = B.topk_select_ex(x, rows, n, stride, lt, k, vptr, iptr, ws, None, split,
+                              flags=flags, **kw)
+    else:
+        rc = int(lib.topk_select_ex(x.data_ptr(), rows, n, stride, B._ptr(lt), k, vptr, iptr,
+                                    ws.data_ptr(), None, split,
+                                    kw.get("seed", 0x5EEDC0DE1234ABCD), flags))
     assert rc == 0, f"topk_select_ex returned {rc}"
     torch.cuda.synchronize()
     v = vbuf.cpu().numpy()

@@ -12,14 +12,14 @@ import sys
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _run_reference(extra_env=None, workload="c1"):
+def _run_reference(extra_env=None, workload="c1", gpus=1):
     env = dict(os.environ)
     for name in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
         env.pop(name, None)
     env.update(extra_env or {})
     return subprocess.run(
         [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
-         workload, "--steps", "2", "--warmup", "3"],
+         workload, "--steps", "2", "--warmup", "3", "--gpus", str(gpus)],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
 
@@ -51,13 +51,22 @@ def test_reference_line_has_the_contract_keys():
 
 def test_reference_under_two_ranks_prints_on_rank_zero_only():
     base = {"WORLD_SIZE": "2", "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": "29581"}
-    r1 = _run_reference({**base, "RANK": "1", "LOCAL_RANK": "1"})
+    r1 = _run_reference({**base, "RANK": "1", "LOCAL_RANK": "1"}, gpus=2)
     assert r1.returncode == 0, r1.stderr[-2000:]
     assert _json_lines(r1.stdout) == []
-    r0 = _run_reference({**base, "RANK": "0", "LOCAL_RANK": "0"})
+    r0 = _run_reference({**base, "RANK": "0", "LOCAL_RANK": "0"}, gpus=2)
     assert r0.returncode == 0, r0.stderr[-2000:]
     lines = _json_lines(r0.stdout)
     assert len(lines) == 1 and lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+
+
+def test_bench_gpus_must_match_the_ranks():
+    """--gpus N names the ranks the run has: N > 1 without torchrun's ranks
+    (or a rank count that differs) is an error, not a silent one-GPU run."""
+    out = _run_reference(gpus=2)
+    assert out.returncode != 0 and "--gpus" in out.stderr
+    out = _run_reference({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"}, gpus=4)
+    assert out.returncode != 0 and "--gpus" in out.stderr
 
 
 def test_bench_rejects_fewer_than_three_warmup_steps():
