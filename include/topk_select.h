@@ -220,7 +220,7 @@ int topk_visit_order(int32_t m, int32_t row, int64_t first_unit,
  * read (a CTA's stamps: the latest call).
  */
 #define TOPK_TIMELINE_CTAS 512
-#define TOPK_TIMELINE_SLOTS 64
+#define TOPK_TIMELINE_SLOTS 128
 int topk_timeline_read(unsigned long long* host_out, void* stream);
 
 /*

@@ -30,7 +30,7 @@ TOPK_POOL_BLOCK = 8
 TOPK_FLAG_IDENTITY_ORDER = 1
 TOPK_FLAG_TEST_STALL = 256
 TOPK_TIMELINE_CTAS = 512
-TOPK_TIMELINE_SLOTS = 64
+TOPK_TIMELINE_SLOTS = 128
 TOPK_MAX_K = 2048
 
 # Every symbol the header exports, with (restype, argtypes).

@@ -143,8 +143,9 @@ constexpr uint64_t kDefaultSeed = 0x5EEDC0DE1234ABCDull;
 #ifndef TOPK_TIMELINE
 #define TOPK_TIMELINE 0
 #endif
-constexpr int kTlSlots = 64;   // u64 slots per CTA
+constexpr int kTlSlots = 128;  // u64 slots per CTA
 constexpr int kTlPieces = 8;   // pieces recorded per CTA
+constexpr int kTlPerPiece = 8; // slots per piece
 enum TlSlot : int {
   kTlStart = 0,       // kernel entry
   kTlSetup = 1,       // after the set-up barrier
@@ -155,12 +156,20 @@ enum TlSlot : int {
   kTlFiltExit = 6,    // filter warp 0: done
   kTlSelExit = 7,     // selectors: done
   kTlInfo = 8,        // SM id | pieces << 32
-  kTlPiece0 = 10,     // per piece p: 4 slots from kTlPiece0 + 4p:
+  kTlProdPiece = 9,   // producer: first piece planned
+  kTlProdOrder = 10,  // producer: its first visiting order drawn
+  kTlWarmEnter = 11,  // selectors: first warm start entered
+  kTlWarmUnit0 = 12,  // ... its first unit read and the warps' keys shared
+  kTlWarmCount = 13,  // ... the sample counted
+  kTlWarmSecond = 14, // ... a second round counted (if one ran)
+  kTlPiece0 = 16,     // per piece p: kTlPerPiece slots from kTlPiece0 + 8p:
                       //   +0 starting threshold published, +1 filter warp 0
                       //   takes its first stage, +2 filter warp 0 releases its
                       //   last stage, +3 selectors done with it (row written
-                      //   or partial list published; a leader after its merge)
-  kTlCyc0 = 48,       // cycle accumulators, see TlCyc
+                      //   or partial list published; a leader after its merge),
+                      //   +4 final tray sort and merge done, +5 ticket taken,
+                      //   +6 leader: partner lists merged
+  kTlCyc0 = kTlPiece0 + kTlPieces * kTlPerPiece,  // cycle accumulators, see TlCyc
 };
 enum TlCyc : int {
   kCycFiltWaitFull = 0,  // filter warp 0: waiting for a stage to land
@@ -177,9 +186,14 @@ enum TlCyc : int {
   kCycSelLeader,         // selectors: leader merges (a count)
   kCycProdWaitEmpty,     // producer: waiting for a free ring stage
   kCycSelRescan,         // selectors: rescans (a count)
+  kCycFiltBody,          // filter warp 0: a stage from landed to released
+  kCycCandClassify,      // filter warp 0: candidate path, classifying the flagged groups
+  kCycCandReserve,       // filter warp 0: candidate path, reserving inbox slots
+  kCycCandWrite,         // filter warp 0: candidate path, writing the words
+  kCycCandWords,         // filter warp 0: words its lanes wrote (a count)
   kCycCount
 };
-static_assert(kTlPiece0 + 4 * kTlPieces <= kTlCyc0 && kTlCyc0 + kCycCount <= kTlSlots,
+static_assert(kTlPiece0 + kTlPerPiece * kTlPieces <= kTlCyc0 && kTlCyc0 + kCycCount <= kTlSlots,
               "timeline slots");
 
 #if TOPK_TIMELINE
@@ -204,7 +218,7 @@ __device__ unsigned long long g_timeline[kTlCtas * kTlSlots];
   } while (0)
 #define TL_PIECE(pc, off)                                   \
   do {                                                      \
-    if ((pc) >= 0 && (pc) < kTlPieces) TL_SET(kTlPiece0 + 4 * (pc) + (off), tl_now()); \
+    if ((pc) >= 0 && (pc) < kTlPieces) TL_SET(kTlPiece0 + kTlPerPiece * (pc) + (off), tl_now()); \
   } while (0)
 #define TL_CYC_DECL(name) unsigned long long name[kCycCount] = {}
 #define TL_CLK(var) const long long var = clock64()
@@ -944,6 +958,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
     copied = waligned ? (d.nvalid & ~3u) : 0u;
   };
   if (stt == 0) st.warm_cnt = 0u;
+  if (stt == 0 && w == 0) TL_SET(kTlWarmEnter, tl_now());
   uint32_t mk = 0u;
   uint64_t spec = 0ull;  // speculative threshold word (0: none)
   bool decided = false;
@@ -1001,6 +1016,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
         st.spec_cnt[4] = 0u;
       }
       Sel::sync();
+      if (stt == 0 && w == 0) TL_SET(kTlWarmUnit0, tl_now());
       // the three smallest warp maxima
       uint32_t s8 = 0xFFFFFFFFu, s7 = 0xFFFFFFFFu, s6 = 0xFFFFFFFFu;
 #pragma unroll
@@ -1067,6 +1083,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
           st.est4[swarp] = umin;
         }
         Sel::sync();
+        if (stt == 0 && w == 0) TL_SET(kTlWarmCount, tl_now());
         const uint32_t n8 = st.spec_cnt[0] & 0xFFFFu, n7 = st.spec_cnt[0] >> 16,
                        n6 = st.spec_cnt[1];
         // the other sample units (not the first, where the candidates come
@@ -1123,6 +1140,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
             c2 = __reduce_add_sync(0xFFFFFFFFu, c2);
             if (lane == 0) atomicAdd(&st.spec_cnt[2], c2);
             Sel::sync();
+            if (stt == 0 && w == 0) TL_SET(kTlWarmSecond, tl_now());
             if (st.spec_cnt[2] >= need) {
               sk = s2;
               nk = st.spec_cnt[2];
@@ -1405,6 +1423,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       Piece pc;
       bool bad_len;
       const int got = get_piece(p, pi, pc, bad_len);
+      if (lane == 0 && pi == 0) TL_SET(kTlProdPiece, tl_now());
       if (lane == 0 && bad_len) atomicOr(p.status, TOPK_STATUS_BAD_LENGTH);
       if (got == 0) break;
       if (got == 2) continue;
@@ -1447,6 +1466,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         const int cs = min(nu - c0, kPermChunk);
         build_visit_order_warp(perm, cs, int64_t(pc.u_begin) + c0, pc.r, p.seed_lo, p.seed_hi,
                                identity, lane);
+        if (lane == 0 && seq == 0 && c0 == 0) TL_SET(kTlProdOrder, tl_now());
         if (lane == 0) {
           // Full units first (the warm start reads the first wu units): if
           // the row's short last unit is among them and the piece has more,
@@ -1550,6 +1570,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       TL_CLK(cw);
       if (!mbar_wait_sleep(&full[stage], phase, wl, 32)) timed_out = true;
       if (tl0) TL_ACC(tlc, kCycFiltWaitFull, cw);
+      TL_CLK(cbody);
       const StageDesc d = desc[stage];
       if (__any_sync(0xFFFFFFFFu, timed_out)) {
         timed_out = true;
@@ -1632,6 +1653,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         // A strict float compare is already the exact word test for every
         // value except NaN and values equal to the threshold's own (ties,
         // and -0.0 against +0.0): those few get the 64-bit word test.
+        TL_CLK(ccl);
         uint32_t passm = 0;
         for (uint32_t gg = gm; gg; gg &= gg - 1u) {
           const int u = __ffs(gg) - 1;
@@ -1660,6 +1682,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         }
         passm &= valid;
         const uint32_t np = __popc(passm);
+#if TOPK_TIMELINE
+        __syncwarp();
+        if (tl0) TL_ACC(tlc, kCycCandClassify, ccl);
+        const long long cres = clock64();
+        const unsigned long long tl_words = __reduce_add_sync(0xFFFFFFFFu, np);
+        if (tl0) tlc[kCycCandWords] += tl_words;
+#endif
         if (np) {
           uint32_t pos = atomicAdd(&st.tail[par], np);
           admitted += np;
@@ -1676,6 +1705,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               __nanosleep(64);
             }
           }
+#if TOPK_TIMELINE
+          if (tl0) TL_ACC(tlc, kCycCandReserve, cres);
+#endif
           volatile uint64_t* ib = par ? inbox1 : inbox0;
           for (uint32_t mm = passm; mm; mm &= mm - 1u) {
             const int e = __ffs(mm) - 1;
@@ -1683,6 +1715,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             ++pos;
           }
         }
+#if TOPK_TIMELINE
+        __syncwarp();
+        if (tl0) TL_ACC(tlc, kCycCandWrite, cres);
+#endif
       }
       if (tl0) TL_ACC(tlc, kCycFiltCand, cc);
       __syncwarp();
@@ -1690,6 +1726,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         mbar_arrive(&empty[stage]);
         if (warp == 0) *reinterpret_cast<volatile uint32_t*>(&st.fprog) = ++released;
       }
+      if (tl0) TL_ACC(tlc, kCycFiltBody, cbody);
       if (tl0 && (d.tag & kLast)) TL_PIECE(tl_piece, 2);
       if (d.tag & kLast) {
         __syncwarp();
@@ -1770,11 +1807,28 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         const uint64_t hmask = pass == 0 ? 0ull : (~0ull << (shift + 8));
         for (int b = stt; b < 256; b += kNST) hist[b] = 0u;
         Sel::sync();
-        // the kept list holds its kept_n real words first
+        // the kept list holds its kept_n real words first.  Words that share
+        // the digit are common (the top of a row sits in a narrow range, and
+        // a pass after the first only sees one bin's words): when every
+        // counted word of the warp falls in one bin, one lane adds them all.
         const int nw = kept_n + tray_n;
-        for (int j = stt; j < nw; j += kNST) {
-          const uint64_t w = j < kept_n ? kept[j] : tray[j - kept_n];
-          if ((w & hmask) == prefix) atomicAdd(&hist[uint32_t(w >> shift) & 0xFFu], 1u);
+        for (int j0 = 0; j0 < nw; j0 += kNST) {
+          const int j = j0 + stt;
+          bool in = false;
+          uint32_t bin = 0u;
+          if (j < nw) {
+            const uint64_t w = j < kept_n ? kept[j] : tray[j - kept_n];
+            in = (w & hmask) == prefix;
+            bin = uint32_t(w >> shift) & 0xFFu;
+          }
+          const uint32_t inm = __ballot_sync(0xFFFFFFFFu, in);
+          if (inm == 0u) continue;
+          const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, bin, __ffs(inm) - 1);
+          if (__all_sync(0xFFFFFFFFu, !in || bin == b0)) {
+            if (lane == __ffs(inm) - 1) atomicAdd(&hist[b0], uint32_t(__popc(inm)));
+          } else if (in) {
+            atomicAdd(&hist[bin], 1u);
+          }
         }
         Sel::sync();
         if (swarp == 0) {
@@ -2148,6 +2202,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         process_tray(true, true, pc);
       }
     }
+    if (stt == 0) TL_PIECE(j, 4);
     // A row whose pieces started from speculative thresholds is selected
     // again if its k-th word does not lie above the largest of them.
     bool redo = false;
@@ -2176,6 +2231,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (stt == 0) {
         const uint32_t t = atomicAdd(&p.tickets[pc.r], 1u);
         st.leader = (t == uint32_t(pc.contributors - 1)) ? 1 : 0;
+        TL_PIECE(j, 5);
       }
       Sel::sync();
       if (st.leader) {
@@ -2248,6 +2304,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             }
           }
         }
+        if (stt == 0) TL_PIECE(j, 6);
         // the row's k-th word must lie above every speculative threshold its
         // pieces started from, else the row is selected again
         const uint64_t wk = slots[k - 1];

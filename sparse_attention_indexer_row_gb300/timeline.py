@@ -21,15 +21,21 @@ from . import binding as B
 from . import build
 
 SLOT = {"start": 0, "setup": 1, "first_copy": 2, "last_copy": 3, "prod_exit": 4,
-        "filt_first": 5, "filt_exit": 6, "sel_exit": 7, "info": 8}
-PIECE0 = 10
+        "filt_first": 5, "filt_exit": 6, "sel_exit": 7, "info": 8, "prod_piece": 9,
+        "prod_order": 10, "warm_enter": 11, "warm_unit0": 12, "warm_count": 13,
+        "warm_second": 14}
+PIECE0 = 16
 PIECES = 8
-CYC0 = 48
+PER_PIECE = 8
+CYC0 = PIECE0 + PIECES * PER_PIECE
 CYC = ["filt_wait_full", "filt_wait_theta", "filt_cand", "filt_stages", "filt_cand_stages",
        "sel_warm", "sel_take", "sel_prune", "sel_sort", "sel_end", "sel_poll", "sel_leaders",
-       "prod_wait_empty", "sel_rescans"]
-COUNTS = {"filt_stages", "filt_cand_stages", "sel_leaders", "sel_rescans"}
-PIECE_EVENTS = ["theta", "filt_first", "filt_last", "sel_done"]
+       "prod_wait_empty", "sel_rescans", "filt_body", "cand_classify", "cand_reserve",
+       "cand_write", "cand_words"]
+COUNTS = {"filt_stages", "filt_cand_stages", "sel_leaders", "sel_rescans", "cand_words"}
+# per-piece events: +0 threshold published, +1 filters' first stage, +2 filters'
+# last release, +3 selectors done, +4 final sort done, +5 ticket taken,
+# +6 leader's merge done
 
 
 def load():
@@ -77,26 +83,33 @@ def summarize(table: np.ndarray, sm_mhz: float) -> dict:
         return (v[v > 0] - t0) / 1e3
 
     out = {"ctas": int(used.size)}
-    for name in ("start", "setup", "first_copy", "filt_first", "last_copy", "filt_exit",
-                 "sel_exit", "prod_exit"):
+    for name in ("start", "setup", "prod_piece", "prod_order", "first_copy", "warm_enter",
+                 "warm_unit0", "warm_count", "warm_second", "filt_first", "last_copy",
+                 "filt_exit", "sel_exit", "prod_exit"):
         out[name] = _stats(rel(SLOT[name]))
     ends = np.maximum.reduce([t[:, SLOT["filt_exit"]], t[:, SLOT["sel_exit"]],
                               t[:, SLOT["prod_exit"]]])
     out["span_us"] = round(float((ends.max() - t0) / 1e3), 2)
     pieces = (t[:, SLOT["info"]] >> 32).astype(np.int64)
     out["pieces_per_cta"] = _stats(pieces)
-    # per piece: threshold published after its first stage could have started,
-    # and the selectors' finish after the filters' last stage
-    theta_first, end_lag = [], []
+    theta_first = []
+    lag = {"final": [], "ticket": [], "leader": [], "done": []}
     for p in range(PIECES):
-        base = PIECE0 + 4 * p
-        th, ff, fl, sd = (t[:, base + i] for i in range(4))
-        ok = (th > 0) & (ff > 0)
-        theta_first.extend(((th[ok] - t0) / 1e3).tolist() if p == 0 else [])
-        ok2 = (fl > 0) & (sd > 0)
-        end_lag.extend(((sd[ok2] - fl[ok2]) / 1e3).tolist())
+        base = PIECE0 + PER_PIECE * p
+        th, ff, fl, sd, fs, tk, ld = (t[:, base + i] for i in range(7))
+        if p == 0:
+            ok = th > 0
+            theta_first.extend(((th[ok] - t0) / 1e3).tolist())
+        ok = (fl > 0) & (fs > 0)
+        lag["final"].extend(((fs[ok] - fl[ok]) / 1e3).tolist())
+        ok = (fs > 0) & (tk > 0)
+        lag["ticket"].extend(((tk[ok] - fs[ok]) / 1e3).tolist())
+        ok = (tk > 0) & (ld > 0)
+        lag["leader"].extend(((ld[ok] - tk[ok]) / 1e3).tolist())
+        ok = (fl > 0) & (sd > 0)
+        lag["done"].extend(((sd[ok] - fl[ok]) / 1e3).tolist())
     out["first_theta"] = _stats(theta_first)
-    out["piece_end_lag"] = _stats(end_lag)
+    out["piece_end"] = {name: _stats(v) for name, v in lag.items()}
     cyc = {}
     for i, name in enumerate(CYC):
         v = t[:, CYC0 + i].astype(np.float64)
