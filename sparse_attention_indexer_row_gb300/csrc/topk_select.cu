@@ -168,7 +168,7 @@ enum TlSlot : int {
                       //   last stage, +3 selectors done with it (row written
                       //   or partial list published; a leader after its merge),
                       //   +4 final tray sort and merge done, +5 ticket taken,
-                      //   +6 leader: partner lists merged
+                      //   +6 leader: partner lists merged, +7 pre-final sort done
   kTlCyc0 = kTlPiece0 + kTlPieces * kTlPerPiece,  // cycle accumulators, see TlCyc
 };
 enum TlCyc : int {
@@ -191,6 +191,7 @@ enum TlCyc : int {
   kCycCandReserve,       // filter warp 0: candidate path, reserving inbox slots
   kCycCandWrite,         // filter warp 0: candidate path, writing the words
   kCycCandWords,         // filter warp 0: words its lanes wrote (a count)
+  kCycFiltLoad,          // filter warp 0: a stage's loads and folded test (from landed)
   kCycCount
 };
 static_assert(kTlPiece0 + kTlPerPiece * kTlPieces <= kTlCyc0 && kTlCyc0 + kCycCount <= kTlSlots,
@@ -499,9 +500,15 @@ struct CtaState {
   Piece table[kTable];             // piece descriptors, by sequence number
 };
 
-__device__ __forceinline__ int64_t flat_lo(int64_t g, int64_t M, int64_t G) { return g * M / G; }
+// Quotient of non-negative 64-bit values, with the (much shorter) 32-bit
+// division when both fit: the plan arithmetic runs before a CTA's first copy.
+__device__ __forceinline__ int64_t udiv(int64_t a, int64_t b) {
+  if (((uint64_t(a) | uint64_t(b)) >> 32) == 0) return int64_t(uint32_t(a) / uint32_t(b));
+  return a / b;
+}
+__device__ __forceinline__ int64_t flat_lo(int64_t g, int64_t M, int64_t G) { return udiv(g * M, G); }
 __device__ __forceinline__ int32_t flat_cta_of(int64_t b, int64_t M, int64_t G) {
-  return int32_t(((b + 1) * G - 1) / M);
+  return int32_t(udiv((b + 1) * G - 1, M));
 }
 
 // The next item of the queue plan's shared queue, taken by lane 0 for the
@@ -538,9 +545,9 @@ __device__ int get_piece(const Params& p, int32_t pi, Piece& out, bool& bad_len)
       item = int64_t(queue_take(p.queue, uint32_t(total)));
     }
     if (item >= total) return 0;
-    const int32_t rank = int32_t(item / p.split);
+    const int32_t rank = int32_t(udiv(item, p.split));
     const int32_t r = p.order ? p.order[rank] : rank;
-    const int32_t s = int32_t(item % p.split);
+    const int32_t s = int32_t(item - int64_t(rank) * p.split);
     int64_t L = p.lengths ? int64_t(p.lengths[r]) : p.n;
     if (L < 0 || L > p.n) {
       bad_len = s == 0;  // a1: reported once per row
@@ -561,7 +568,7 @@ __device__ int get_piece(const Params& p, int32_t pi, Piece& out, bool& bad_len)
   }
   const int64_t M = int64_t(p.rows) * p.u_full;
   const int64_t lo = flat_lo(cta, M, G), hi = flat_lo(cta + 1, M, G);
-  const int64_t r0 = lo / p.u_full;
+  const int64_t r0 = udiv(lo, p.u_full);
   const int64_t r = r0 + pi;
   const int64_t rs = r * p.u_full;
   if (r >= p.rows || rs >= hi) return 0;
@@ -586,11 +593,9 @@ __device__ int get_piece(const Params& p, int32_t pi, Piece& out, bool& bad_len)
 // lane i % 32, register i / 32; strides of 32 and more swap registers,
 // shorter ones exchange through shuffles.
 template <int E>
-__device__ __forceinline__ void visit_order_sort(uint32_t* perm, int m, int64_t first, int32_t row,
-                                                 uint32_t seed_lo, uint32_t seed_hi,
-                                                 bool identity, int lane) {
-  constexpr int n = 32 * E;
-  uint32_t v[E];
+__device__ __forceinline__ void visit_keys(uint32_t (&v)[E], int m, int64_t first, int32_t row,
+                                           uint32_t seed_lo, uint32_t seed_hi, bool identity,
+                                           int lane) {
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int j = e * 32 + lane;
@@ -606,6 +611,15 @@ __device__ __forceinline__ void visit_order_sort(uint32_t* perm, int m, int64_t 
     }
     v[e] = key;
   }
+}
+
+template <int E>
+__device__ __forceinline__ void visit_order_sort(uint32_t* perm, int m, int64_t first, int32_t row,
+                                                 uint32_t seed_lo, uint32_t seed_hi,
+                                                 bool identity, int lane) {
+  constexpr int n = 32 * E;
+  uint32_t v[E];
+  visit_keys<E>(v, m, first, row, seed_lo, seed_hi, identity, lane);
 #pragma unroll
   for (int size = 2; size <= n; size <<= 1) {
 #pragma unroll
@@ -646,6 +660,27 @@ __device__ void build_visit_order_warp(uint32_t* perm, int m, int64_t first, int
   else if (m <= 64) visit_order_sort<2>(perm, m, first, row, seed_lo, seed_hi, identity, lane);
   else if (m <= 128) visit_order_sort<4>(perm, m, first, row, seed_lo, seed_hi, identity, lane);
   else visit_order_sort<8>(perm, m, first, row, seed_lo, seed_hi, identity, lane);
+}
+
+// The first nhead entries of the same order (its nhead smallest keys), found
+// by warp minima without the sort, into perm[0, nhead): nhead <= m <= 64.
+// The keys are distinct (their low bits are the positions), so the q-th
+// smallest is the smallest key above the (q-1)-th.
+__device__ void visit_order_head(uint32_t* perm, int m, int64_t first, int32_t row,
+                                 uint32_t seed_lo, uint32_t seed_hi, bool identity, int lane,
+                                 int nhead) {
+  uint32_t v[2];
+  visit_keys<2>(v, m, first, row, seed_lo, seed_hi, identity, lane);
+  uint32_t prev = 0u;
+  for (int q = 0; q < nhead; ++q) {
+    uint32_t lm = 0xFFFFFFFFu;
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      if (q == 0 || v[e] > prev) lm = min(lm, v[e]);
+    prev = __reduce_min_sync(0xFFFFFFFFu, lm);
+    if (lane == 0) perm[q] = prev;
+  }
+  __syncwarp();
 }
 
 // Bitonic network, largest first, over the n = T::size * E words a[0, n),
@@ -1464,14 +1499,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       const int wu = warm_units(p.k, nu, pc.L);
       for (int c0 = 0; c0 < nu; c0 += kPermChunk) {
         const int cs = min(nu - c0, kPermChunk);
-        build_visit_order_warp(perm, cs, int64_t(pc.u_begin) + c0, pc.r, p.seed_lo, p.seed_hi,
-                               identity, lane);
-        if (lane == 0 && seq == 0 && c0 == 0) TL_SET(kTlProdOrder, tl_now());
-        if (lane == 0) {
-          // Full units first (the warm start reads the first wu units): if
-          // the row's short last unit is among them and the piece has more,
-          // swap it with the unit after them.
-          if (c0 == 0 && cs > wu && partial_tail) {
+        // Full units first (the warm start reads the first wu units): if the
+        // row's short last unit is among them and the piece has more, swap
+        // it with the unit after them.
+        const bool head_first = c0 == 0 && cs > wu;
+        auto fix_head = [&]() {
+          if (head_first && partial_tail) {
             for (int q = 0; q < wu; ++q) {
               if (pc.u_begin + int(perm[q] & uint32_t(kPermChunk - 1)) == m_row - 1) {
                 const uint32_t t0 = perm[q];
@@ -1480,7 +1513,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               }
             }
           }
-          for (int i = 0; i < cs; ++i) {
+        };
+        // lane 0: the copies of order positions [i0, i1) of this chunk
+        auto issue = [&](int i0, int i1) {
+          for (int i = i0; i < i1 && !stalled; ++i) {
             if (int64_t(g) == int64_t(p.stall_at)) {
               // test only: stop in front of this stage for good (its full
               // barrier never completes, so the waits behind it run out)
@@ -1513,6 +1549,26 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             if (c0 + i == wu - 1) *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
             advance();
           }
+        };
+        // The piece's first units are the smallest keys of its first chunk:
+        // for chunks of up to 64 units their copies go out (phase 0) before
+        // the rest of the order is sorted (phase 1).
+        const bool early = head_first && cs <= 64;
+        for (int ph = early ? 0 : 1; ph < 2 && !stalled; ++ph) {
+          if (ph == 0) {
+            visit_order_head(perm, cs, int64_t(pc.u_begin) + c0, pc.r, p.seed_lo, p.seed_hi,
+                             identity, lane, wu + 1);
+          } else {
+            build_visit_order_warp(perm, cs, int64_t(pc.u_begin) + c0, pc.r, p.seed_lo,
+                                   p.seed_hi, identity, lane);
+            if (lane == 0 && seq == 0 && c0 == 0) TL_SET(kTlProdOrder, tl_now());
+          }
+          if (lane == 0) {
+            fix_head();
+            issue(ph == 0 ? 0 : (early ? wu : 0), ph == 0 ? wu : cs);
+          }
+          __syncwarp();
+          stalled = __shfl_sync(0xFFFFFFFFu, stalled, 0);
         }
         __syncwarp();  // the order buffer is reused by the next chunk
         stalled = __shfl_sync(0xFFFFFFFFu, stalled, 0);
@@ -1644,6 +1700,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         return __float_as_uint(__ldg(row + e0 + pos));
       };
       if (tl0) TL_CNT(tlc, kCycFiltStages);
+      if (tl0) TL_ACC(tlc, kCycFiltLoad, cbody);
       TL_CLK(cc);
       if (__any_sync(0xFFFFFFFFu, gm != 0u)) {
         if (tl0) TL_CNT(tlc, kCycFiltCandStages);
@@ -1807,28 +1864,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         const uint64_t hmask = pass == 0 ? 0ull : (~0ull << (shift + 8));
         for (int b = stt; b < 256; b += kNST) hist[b] = 0u;
         Sel::sync();
-        // the kept list holds its kept_n real words first.  Words that share
-        // the digit are common (the top of a row sits in a narrow range, and
-        // a pass after the first only sees one bin's words): when every
-        // counted word of the warp falls in one bin, one lane adds them all.
+        // the kept list holds its kept_n real words first
         const int nw = kept_n + tray_n;
-        for (int j0 = 0; j0 < nw; j0 += kNST) {
-          const int j = j0 + stt;
-          bool in = false;
-          uint32_t bin = 0u;
-          if (j < nw) {
-            const uint64_t w = j < kept_n ? kept[j] : tray[j - kept_n];
-            in = (w & hmask) == prefix;
-            bin = uint32_t(w >> shift) & 0xFFu;
-          }
-          const uint32_t inm = __ballot_sync(0xFFFFFFFFu, in);
-          if (inm == 0u) continue;
-          const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, bin, __ffs(inm) - 1);
-          if (__all_sync(0xFFFFFFFFu, !in || bin == b0)) {
-            if (lane == __ffs(inm) - 1) atomicAdd(&hist[b0], uint32_t(__popc(inm)));
-          } else if (in) {
-            atomicAdd(&hist[bin], 1u);
-          }
+        for (int j = stt; j < nw; j += kNST) {
+          const uint64_t w = j < kept_n ? kept[j] : tray[j - kept_n];
+          if ((w & hmask) == prefix) atomicAdd(&hist[uint32_t(w >> shift) & 0xFFu], 1u);
         }
         Sel::sync();
         if (swarp == 0) {
@@ -2115,7 +2155,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           // the filters wait on the next piece's threshold, not on this
           // piece's end: a warm start whose units are on their way goes first
           if (done && warm_due) done = 0;
-          if (pc.contributors > 1) {
+          // (the row's shared word is in global memory: an L2 round trip,
+          // so it is looked at on every fourth poll only)
+          if (pc.contributors > 1 && (it & 3u) == 0u) {
             const unsigned long long gt =
                 *reinterpret_cast<volatile unsigned long long*>(&p.row_theta[pc.r]);
             if (gt > theta) atomicMax(&st.theta[par], gt);
@@ -2167,6 +2209,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         TL_CLK(cs);
         if (tray_n > 0) process_tray(true, true, pc);
         if (stt == 0) TL_ACC(tlc, kCycSelSort, cs);
+        if (stt == 0) TL_PIECE(j, 7);
         continue;
       }
       if (done) break;
@@ -2260,7 +2303,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             } else {
               const int64_t M = int64_t(p.rows) * p.u_full, G = gridDim.x;
               const int64_t go = pc.first_cta + o;
-              slot = 2 * go + (flat_lo(go, M, G) / p.u_full == pc.r ? 0 : 1);
+              slot = 2 * go + (udiv(flat_lo(go, M, G), p.u_full) == pc.r ? 0 : 1);
             }
             if (!IN_BOUNDS(slot >= 0 && slot < p.nslots, p.status)) slot = 0;
             st.gsrc[stt] = p.partials + slot * kp;

@@ -31,11 +31,11 @@ CYC0 = PIECE0 + PIECES * PER_PIECE
 CYC = ["filt_wait_full", "filt_wait_theta", "filt_cand", "filt_stages", "filt_cand_stages",
        "sel_warm", "sel_take", "sel_prune", "sel_sort", "sel_end", "sel_poll", "sel_leaders",
        "prod_wait_empty", "sel_rescans", "filt_body", "cand_classify", "cand_reserve",
-       "cand_write", "cand_words"]
+       "cand_write", "cand_words", "filt_load"]
 COUNTS = {"filt_stages", "filt_cand_stages", "sel_leaders", "sel_rescans", "cand_words"}
 # per-piece events: +0 threshold published, +1 filters' first stage, +2 filters'
 # last release, +3 selectors done, +4 final sort done, +5 ticket taken,
-# +6 leader's merge done
+# +6 leader's merge done, +7 pre-final sort done
 
 
 def load():
@@ -93,10 +93,12 @@ def summarize(table: np.ndarray, sm_mhz: float) -> dict:
     pieces = (t[:, SLOT["info"]] >> 32).astype(np.int64)
     out["pieces_per_cta"] = _stats(pieces)
     theta_first = []
-    lag = {"final": [], "ticket": [], "leader": [], "done": []}
+    lag = {"prefinal_before_last": [], "final": [], "ticket": [], "leader": [], "done": []}
     for p in range(PIECES):
         base = PIECE0 + PER_PIECE * p
-        th, ff, fl, sd, fs, tk, ld = (t[:, base + i] for i in range(7))
+        th, ff, fl, sd, fs, tk, ld, pf = (t[:, base + i] for i in range(8))
+        ok = (fl > 0) & (pf > 0)
+        lag["prefinal_before_last"].extend(((fl[ok] - pf[ok]) / 1e3).tolist())
         if p == 0:
             ok = th > 0
             theta_first.extend(((th[ok] - t0) / 1e3).tolist())
