@@ -198,9 +198,12 @@ int topk_ws_stats(void* ws, int32_t rows, int64_t n, int32_t k, int32_t split,
  * Given the chunk's row, its first unit index in the row and the seed, the
  * order is the chunk's units sorted by (Philox4x32-10(counter =
  * (first_unit + j, row, 0, 0), key = seed) word 0 with its low 8 bits
- * cleared, j).  (When a row's short last unit would come first in its piece,
- * the kernel swaps the first two entries, so that the warm start reads a full
- * unit; this call reports the order before that swap.)  Enqueued on `stream`.
+ * cleared, j).  (The kernel keeps a row's short last unit out of the first
+ * units of a piece, which its warm start reads: if it is among the first w of
+ * a longer piece -- w = 3 for k <= 512, else up to 4 -- it trades places with
+ * the entry after them, and in a piece of at most w units it trades places
+ * with the last entry.  This call reports the order before that swap.)
+ * Enqueued on `stream`.
  * Returns TOPK_ERR_ARG for m outside [1, 256], a negative first_unit or a
  * NULL order_out.
  */

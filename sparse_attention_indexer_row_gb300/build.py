@@ -2,7 +2,8 @@
 
 Two instrumented variants come from the same sources with one macro each:
 ``libtopk_gb300_timeline.so`` (``-DTOPK_TIMELINE=1``: per-CTA global-timer
-stamps and cycle counts, read with ``topk_timeline_read``) and
+stamps, read with ``topk_timeline_read``; level 2 adds per-activity cycle
+counts, which slow the filter loop) and
 ``libtopk_gb300_debug.so`` (``-DTOPK_DEBUG_BOUNDS=1``: every shared- and
 global-memory index the selection computes is checked before use; a bad one
 sets ``TOPK_STATUS_BOUNDS`` and the access is skipped).  The product library

@@ -134,12 +134,13 @@ constexpr int kMinSegUnits = 4;    // at least 128 KB per split segment
 constexpr uint64_t kDefaultSeed = 0x5EEDC0DE1234ABCDull;
 
 // ---------------------------------------------------------------------------
-// Timeline (an instrumented build only: compiled with -DTOPK_TIMELINE=1).
+// Timeline (an instrumented build only: compiled with -DTOPK_TIMELINE=1 or 2).
 // Each CTA of the selection kernel stamps the global timer at the events
-// below and accumulates SM cycles per activity of one thread of each role
-// (producer lane 0, filter warp 0 lane 0, selector thread 0) into its row of
-// g_timeline; topk_timeline_read copies the table out.  In the normal build
-// every TL_* macro is empty and the table does not exist.
+// below into its row of g_timeline; with level 2 it also accumulates SM
+// cycles per activity of one thread of each role (producer lane 0, filter
+// warp 0 lane 0, selector thread 0).  topk_timeline_read copies the table
+// out.  In the normal build every TL_* macro is empty and the table does not
+// exist.
 #ifndef TOPK_TIMELINE
 #define TOPK_TIMELINE 0
 #endif
@@ -221,6 +222,9 @@ __device__ unsigned long long g_timeline[kTlCtas * kTlSlots];
   do {                                                      \
     if ((pc) >= 0 && (pc) < kTlPieces) TL_SET(kTlPiece0 + kTlPerPiece * (pc) + (off), tl_now()); \
   } while (0)
+#if TOPK_TIMELINE >= 2
+// level 2: cycle accumulators as well (they slow the filter loop noticeably)
+#define TL_CYCLES 1
 #define TL_CYC_DECL(name) unsigned long long name[kCycCount] = {}
 #define TL_CLK(var) const long long var = clock64()
 #define TL_ACC(arr, which, since) ((arr)[which] += (unsigned long long)(clock64() - (since)))
@@ -230,9 +234,13 @@ __device__ unsigned long long g_timeline[kTlCtas * kTlSlots];
     for (int q_ = 0; q_ < kCycCount; ++q_)                              \
       if ((arr)[q_]) TL_SET(kTlCyc0 + q_, (arr)[q_]);                   \
   } while (0)
+#endif
 #else
 #define TL_SET(slot, v) ((void)0)
 #define TL_PIECE(pc, off) ((void)0)
+#endif
+#ifndef TL_CYCLES
+#define TL_CYCLES 0
 #define TL_CYC_DECL(name) [[maybe_unused]] int name = 0
 #define TL_CLK(var) ((void)0)
 #define TL_ACC(arr, which, since) ((void)(arr))
@@ -264,6 +272,9 @@ __device__ __forceinline__ bool bounds_ok(bool ok, uint32_t* status) {
 constexpr int kNF = 8;
 constexpr int kNS = 8;
 constexpr int kNFT = kNF * 32;                   // filter threads
+constexpr int kFG = 2;                           // filter groups (alternate ring stages)
+constexpr int kGW = kNF / kFG;                   // warps per filter group
+constexpr int kGT = kGW * 32;                    // threads per filter group
 constexpr int kNST = kNS * 32;                   // selector threads
 constexpr int kThreads = kNFT + kNST + 32;
 constexpr int kProducerWarp = kNF + kNS;
@@ -274,8 +285,9 @@ constexpr int kTray = 3072;                      // tray words
 constexpr int kTable = 16;                       // piece descriptors in flight
 // Inbox words the selectors move per step.  A take must never reach a slot
 // reserved by a filter lane that is itself waiting for room, so it stays at
-// least one lane-stage reservation (kEPT words) short of the inbox size.
-constexpr int kTakeMax = (kInbox - kEPT) < 1024 ? (kInbox - kEPT) : 1024;
+// least one lane-stage reservation (2 kEPT words: a filter lane tests 64
+// elements of a stage) short of the inbox size.
+constexpr int kTakeMax = (kInbox - 2 * kEPT) < 1024 ? (kInbox - 2 * kEPT) : 1024;
 // Smallest batch the selectors take while the piece's filters are still
 // running (a prune needs kPruneStep new words anyway); polling for less only
 // takes issue slots from the filter warps.
@@ -426,6 +438,8 @@ constexpr uint32_t kSeqMask = 0x0FFFFFFFu;
 constexpr uint32_t kFirst = 1u << 28;  // the piece's first stage
 constexpr uint32_t kLast = 1u << 29;   // the piece's last stage
 constexpr uint32_t kEnd = 1u << 30;    // no more stages
+constexpr uint32_t kLastG = 1u << 31;  // a filter group's last stage of the piece (the
+                                       // piece's last two stages, or its only one)
 
 // A piece: units [u_begin, u_end) of row r, processed with one tray.
 struct Piece {
@@ -474,7 +488,7 @@ __host__ __device__ inline SmemLayout smem_layout(int kp) {
 struct CtaState {
   uint32_t head[2];          // inbox p: next word the selectors take
   uint32_t tail[2];          // inbox p: next word a filter warp reserves
-  int fdone[2];              // filter warps done with pieces of parity p (cumulative)
+  int fdone[2];              // filter warps' stage reports for pieces of parity p (cumulative)
   int sel_pieces;            // pieces the selectors have finished
   int pieces_pub;            // piece descriptors the producer has published
   int npieces;               // total pieces of this CTA, -1 until known
@@ -783,17 +797,20 @@ __device__ __forceinline__ void write_row(const Params& p, int32_t r, const uint
   }
 }
 
-// One thread's share of a stage: elements 4 * (t + 256 u) + c, u < 8, c < 4.
-// A full, aligned unit is read from shared memory only; otherwise elements
-// past the copied prefix come from global memory and elements past the
-// unit's end are marked invalid (bit e of the result clear).
+// One thread's share of a span of T * 32 elements read by T threads:
+// elements 4 * (t + T u) + c, u < 8, c < 4.  A full, aligned span is read
+// from shared memory only; otherwise elements past the copied prefix come
+// from global memory and elements past the span's end are marked invalid
+// (bit e of the result clear).  (T = 256: the selector team's view of a
+// whole unit; T = 128: a filter group's view of half a unit.)
+template <int T = kNFT>
 __device__ __forceinline__ uint32_t load_share(float (&x)[kEPT], const float* src, const float* row,
                                                uint32_t e0, uint32_t nvalid, uint32_t copied,
                                                int t) {
-  if (copied == uint32_t(kUnit)) {
+  if (copied == uint32_t(T * kEPT)) {
 #pragma unroll
     for (int u = 0; u < kF4; ++u) {
-      const float4 v = reinterpret_cast<const float4*>(src)[t + kNFT * u];
+      const float4 v = reinterpret_cast<const float4*>(src)[t + T * u];
       x[4 * u + 0] = v.x;
       x[4 * u + 1] = v.y;
       x[4 * u + 2] = v.z;
@@ -806,7 +823,7 @@ __device__ __forceinline__ uint32_t load_share(float (&x)[kEPT], const float* sr
   for (int u = 0; u < kF4; ++u) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const uint32_t pos = uint32_t(4 * (t + kNFT * u) + c);
+      const uint32_t pos = uint32_t(4 * (t + T * u) + c);
       float v = 0.f;
       if (pos < copied) v = src[pos];
       else if (pos < nvalid) v = __ldg(row + e0 + pos);
@@ -1010,7 +1027,10 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
   const int nu = pw.u_end - pw.u_begin;
   if (wu == warm_cap(k) && nu >= wu) {
     const uint64_t need64 = spec_need(k, wu, pw.L);
-    if (need64 <= kSpecMaxNeed) {
+    // (with the three-unit sample only the warps' largest keys are tried:
+    // rank-R candidates need an exact per-warp select that costs more than a
+    // speculative start saves on rows this short)
+    if (need64 <= (wu == kWarmUnits ? uint64_t(kSpecMaxNeed) : 128ull)) {
       const uint32_t need = uint32_t(need64);
       const int R = need <= 128u ? 1 : int((5u * need + 4u * wu * kNS - 1u) / (4u * wu * kNS));
       float lm = -__int_as_float(0x7F800000);
@@ -1319,6 +1339,7 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
 // the next lane's; its score is the largest of its valid scores (NaN left
 // out; NaN only when every valid score is NaN), +0.0 above -0.0.  Lanes with
 // an even thread index store one float per block of the stage.
+template <int T>
 __device__ __forceinline__ void store_block_max(const float (&x)[kEPT], uint32_t valid, int ft,
                                                 uint32_t e0, uint32_t nvalid, float* brow,
                                                 int64_t bstride, uint32_t* status) {
@@ -1358,13 +1379,13 @@ __device__ __forceinline__ void store_block_max(const float (&x)[kEPT], uint32_t
     }
   }
   if ((ft & 1) == 0) {
-    // block of the float4 pair (ft, ft + 1) in group u: (e0 + 4 ft) / 8 + 128 u
+    // block of the float4 pair (ft, ft + 1) in group u: (e0 + 4 ft) / 8 + (T / 2) u
     float* dst = brow + ((e0 + 4u * uint32_t(ft)) >> 3);
 #pragma unroll
     for (int u = 0; u < kF4; ++u)
-      if (uint32_t(4 * (ft + kNFT * u)) < nvalid &&
-          IN_BOUNDS(int64_t((e0 + 4u * uint32_t(ft)) >> 3) + (kNFT / 2) * u < bstride, status))
-        dst[(kNFT / 2) * u] = bm[u];
+      if (uint32_t(4 * (ft + T * u)) < nvalid &&
+          IN_BOUNDS(int64_t((e0 + 4u * uint32_t(ft)) >> 3) + (T / 2) * u < bstride, status))
+        dst[(T / 2) * u] = bm[u];
   }
 }
 
@@ -1420,7 +1441,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     st.wait_limit = p.wait_limit;
     for (int i = 0; i < nstage; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kNF);
+      mbar_init(&empty[i], kGW);  // the warps of the stage's filter group
     }
     mbar_init_fence();
   }
@@ -1488,7 +1509,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         d.e0 = 0;
         d.nvalid = 0;
         d.r = uint32_t(pc.r);
-        d.tag = uint32_t(seq) | kFirst | kLast;
+        d.tag = uint32_t(seq) | kFirst | kLast | kLastG;
         desc[stage] = d;
         mbar_arrive(&full[stage]);
         *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
@@ -1499,17 +1520,19 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       const int wu = warm_units(p.k, nu, pc.L);
       for (int c0 = 0; c0 < nu; c0 += kPermChunk) {
         const int cs = min(nu - c0, kPermChunk);
-        // Full units first (the warm start reads the first wu units): if the
-        // row's short last unit is among them and the piece has more, swap
-        // it with the unit after them.
+        // Full units first (the warm start reads the first wu units, its
+        // bounds come from the first one): if the row's short last unit is
+        // among them and the piece has more, swap it with the unit after
+        // them; in a piece of at most wu units it is swapped to the end.
         const bool head_first = c0 == 0 && cs > wu;
         auto fix_head = [&]() {
-          if (head_first && partial_tail) {
-            for (int q = 0; q < wu; ++q) {
+          if (c0 == 0 && cs > 1 && partial_tail) {
+            const int to = head_first ? wu : cs - 1;
+            for (int q = 0; q < to; ++q) {
               if (pc.u_begin + int(perm[q] & uint32_t(kPermChunk - 1)) == m_row - 1) {
                 const uint32_t t0 = perm[q];
-                perm[q] = perm[wu];
-                perm[wu] = t0;
+                perm[q] = perm[to];
+                perm[to] = t0;
               }
             }
           }
@@ -1533,7 +1556,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             d.nvalid = nvalid;
             d.r = uint32_t(pc.r);
             d.tag = uint32_t(seq) | (c0 == 0 && i == 0 ? kFirst : 0u) |
-                    (c0 + i == nu - 1 ? kLast : 0u);
+                    (c0 + i == nu - 1 ? kLast : 0u) | (c0 + i >= nu - 2 ? kLastG : 0u);
             desc[stage] = d;
             fence_proxy_async_smem();
             if (bytes) {
@@ -1586,14 +1609,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         if (!mbar_wait(&full[q % uint32_t(nstage)], (q / uint32_t(nstage)) & 1u, wl))
           gave_up = true;
       if (stalled) return;  // (test only: no end marker either)
-      next_slot();
-      StageDesc d;
-      d.e0 = 0;
-      d.nvalid = 0;
-      d.r = 0;
-      d.tag = kEnd;
-      desc[stage] = d;
-      mbar_arrive(&full[stage]);
+      // one end marker for each filter group (consecutive stages alternate)
+      for (int q = 0; q < kFG; ++q) {
+        next_slot();
+        StageDesc d;
+        d.e0 = 0;
+        d.nvalid = 0;
+        d.r = 0;
+        d.tag = kEnd;
+        desc[stage] = d;
+        mbar_arrive(&full[stage]);
+        advance();
+      }
       if (gave_up) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
       TL_FLUSH(tlc);
       TL_SET(kTlInfo, (unsigned long long)smid() | ((unsigned long long)seq << 32));
@@ -1603,26 +1630,33 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   }
 
   // ---------------- filter warps: a4 + a5 ----------------
+  // Two groups of kGW warps take alternate ring stages (group q the stages
+  // g = q, q + 2, ...); a group's 128 threads test a whole 8192-element unit,
+  // 64 elements a thread as two contiguous 4096-element halves.  A warp thus
+  // pays a stage's fixed costs (the wait, the descriptor, the release, and the
+  // candidate path when some lane has a survivor) once for 2048 elements, and
+  // the two groups' latencies overlap.
   if (warp < kNF) {
-    const int ft = tid;  // 0 .. kNFT-1
+    const int grp = warp / kGW;     // filter group
+    const int tg = tid - grp * kGT;  // 0 .. kGT-1 within the group
     uint64_t th = 0ull;
     float thf = threshold_float(th);
     uint32_t admitted = 0;
-    uint32_t released = 0;  // stages released (kept by warp 0 for the selectors)
     bool saw_nan = false, timed_out = false;
-    int stage = 0;
-    uint32_t phase = 0;
+    uint32_t gs = uint32_t(grp);  // global index of the group's next stage
+    int cur_seq = -1;             // piece of the stages seen last
     int par = 0;
     int32_t r = 0;
     const bool tl0 = tid == 0;  // (timeline: filter warp 0, lane 0)
     TL_CYC_DECL(tlc);
-    [[maybe_unused]] int tl_piece = -1;
     (void)tl0;
     const float* row = p.scores;
     bool aligned = true;
     // every exit decision is warp-uniform: a wait that gave up in any lane
     // ends the warp's loop
     for (;;) {
+      const int stage = int(gs % uint32_t(nstage));
+      const uint32_t phase = (gs / uint32_t(nstage)) & 1u;
       TL_CLK(cw);
       if (!mbar_wait_sleep(&full[stage], phase, wl, 32)) timed_out = true;
       if (tl0) TL_ACC(tlc, kCycFiltWaitFull, cw);
@@ -1633,12 +1667,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         break;
       }
       if (d.tag & kEnd) break;
-      if (d.tag & kFirst) {
-        const int seq = int(d.tag & kSeqMask);
+      const int seq = int(d.tag & kSeqMask);
+      if (seq != cur_seq) {
+        // The group's first stage of a piece.  The selectors set the piece's
+        // starting threshold once its first units have landed, and only after
+        // piece seq - 2 (which used the same inbox, counters and threshold
+        // word) is finished.
+        cur_seq = seq;
         par = seq & 1;
-        // The selectors set the piece's starting threshold once this unit
-        // has landed, and only after piece seq - 2 (which used the same
-        // inbox, counters and threshold word) is finished.
         TL_CLK(ct);
         if (lane == 0) {
           uint32_t it = 0;
@@ -1657,7 +1693,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         if (tl0) {
           TL_ACC(tlc, kCycFiltWaitTheta, ct);
           if (seq == 0) TL_SET(kTlFiltFirst, tl_now());
-          tl_piece = seq;
           TL_PIECE(seq, 1);
         }
         r = int32_t(d.r);
@@ -1675,27 +1710,39 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       const float* src = ring + stage * kUnit;
       const uint32_t e0 = d.e0, nvalid = d.nvalid;
       const uint32_t copied = aligned ? (nvalid & ~3u) : 0u;
-      float x[kEPT];
-      const uint32_t valid = load_share(x, src, row, e0, nvalid, copied, ft);  // bit e: in the row
-      if (p.bmax != nullptr)
-        store_block_max(x, valid, ft, e0, nvalid, p.bmax + int64_t(r) * p.bstride, p.bstride,
-                        p.status);
       // Most stages have no element past the threshold: the test first folds
       // each float4 group into one bit (a superset: it also passes NaN, ties
       // and padding); only flagged groups are re-read (where they sit: the
       // stage is not released yet, or past the copied prefix of a ragged
-      // unit, global memory) and classified element by element.
-      uint32_t gm = 0;  // bit u: group u (elements 4u .. 4u+3) may hold a survivor
+      // unit, global memory) and classified element by element.  Group ug
+      // (0 .. 15) of this thread is float4 tg + kGT ug of the unit.
+      uint32_t gm = 0;
+      uint64_t valid = 0;
 #pragma unroll
-      for (int u = 0; u < kF4; ++u)
-        gm |= uint32_t(!(x[4 * u + 0] < thf) | !(x[4 * u + 1] < thf) | !(x[4 * u + 2] < thf) |
-                       !(x[4 * u + 3] < thf)) << u;
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t hb = uint32_t(h) * uint32_t(kUnit / 2);
+        const uint32_t nv_h = nvalid > hb ? min(nvalid - hb, uint32_t(kUnit / 2)) : 0u;
+        const uint32_t cp_h = copied > hb ? min(copied - hb, uint32_t(kUnit / 2)) : 0u;
+        float x[kEPT];
+        const uint32_t vh = load_share<kGT>(x, src + hb, row, e0 + hb, nv_h, cp_h, tg);
+        if (p.bmax != nullptr)
+          store_block_max<kGT>(x, vh, tg, e0 + hb, nv_h, p.bmax + int64_t(r) * p.bstride,
+                               p.bstride, p.status);
+        valid |= uint64_t(vh) << (32 * h);
+#pragma unroll
+        for (int u = 0; u < kF4; ++u)
+          gm |= uint32_t(!(x[4 * u + 0] < thf) | !(x[4 * u + 1] < thf) | !(x[4 * u + 2] < thf) |
+                         !(x[4 * u + 3] < thf)) << (u + kF4 * h);
+      }
+      // element e (0 .. 63) of this thread: unit position 4 (tg + kGT (e / 4)) + e % 4
+      auto pos_of = [&](int e) -> uint32_t {
+        return uint32_t(4 * (tg + kGT * (e >> 2)) + (e & 3));
+      };
       auto word_of = [&](uint32_t bits, int e) -> uint64_t {
-        const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
-        return (uint64_t(order_key(bits)) << 32) | uint64_t(~(e0 + pos));
+        return (uint64_t(order_key(bits)) << 32) | uint64_t(~(e0 + pos_of(e)));
       };
       auto elem_bits = [&](int e) -> uint32_t {
-        const uint32_t pos = uint32_t(4 * (ft + kNFT * (e >> 2)) + (e & 3));
+        const uint32_t pos = pos_of(e);
         if (pos < copied) return __float_as_uint(src[pos]);
         return __float_as_uint(__ldg(row + e0 + pos));
       };
@@ -1711,22 +1758,22 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         // value except NaN and values equal to the threshold's own (ties,
         // and -0.0 against +0.0): those few get the 64-bit word test.
         TL_CLK(ccl);
-        uint32_t passm = 0;
+        uint64_t passm = 0;
         for (uint32_t gg = gm; gg; gg &= gg - 1u) {
-          const int u = __ffs(gg) - 1;
+          const int ug = __ffs(gg) - 1;
           float4 v;
           if (copied == uint32_t(kUnit)) {
-            v = reinterpret_cast<const float4*>(src)[ft + kNFT * u];
+            v = reinterpret_cast<const float4*>(src)[tg + kGT * ug];
           } else {
-            v.x = __uint_as_float(((valid >> (4 * u + 0)) & 1u) ? elem_bits(4 * u + 0) : 0u);
-            v.y = __uint_as_float(((valid >> (4 * u + 1)) & 1u) ? elem_bits(4 * u + 1) : 0u);
-            v.z = __uint_as_float(((valid >> (4 * u + 2)) & 1u) ? elem_bits(4 * u + 2) : 0u);
-            v.w = __uint_as_float(((valid >> (4 * u + 3)) & 1u) ? elem_bits(4 * u + 3) : 0u);
+            v.x = __uint_as_float(((valid >> (4 * ug + 0)) & 1u) ? elem_bits(4 * ug + 0) : 0u);
+            v.y = __uint_as_float(((valid >> (4 * ug + 1)) & 1u) ? elem_bits(4 * ug + 1) : 0u);
+            v.z = __uint_as_float(((valid >> (4 * ug + 2)) & 1u) ? elem_bits(4 * ug + 2) : 0u);
+            v.w = __uint_as_float(((valid >> (4 * ug + 3)) & 1u) ? elem_bits(4 * ug + 3) : 0u);
           }
           const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int e = 4 * u + c;
+            const int e = 4 * ug + c;
             bool pass = vv[c] > thf;
             if (!(vv[c] < thf) && !pass) {  // equal to the threshold's value, or NaN
               const uint32_t bits = __float_as_uint(vv[c]);
@@ -1734,12 +1781,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               saw_nan |= nan && ((valid >> e) & 1u);
               pass = !nan && word_of(bits, e) > th;
             }
-            passm |= uint32_t(pass) << e;
+            passm |= uint64_t(pass) << e;
           }
         }
         passm &= valid;
-        const uint32_t np = __popc(passm);
-#if TOPK_TIMELINE
+        const uint32_t np = uint32_t(__popcll(passm));
+#if TL_CYCLES
         __syncwarp();
         if (tl0) TL_ACC(tlc, kCycCandClassify, ccl);
         const long long cres = clock64();
@@ -1762,17 +1809,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               __nanosleep(64);
             }
           }
-#if TOPK_TIMELINE
+#if TL_CYCLES
           if (tl0) TL_ACC(tlc, kCycCandReserve, cres);
 #endif
           volatile uint64_t* ib = par ? inbox1 : inbox0;
-          for (uint32_t mm = passm; mm; mm &= mm - 1u) {
-            const int e = __ffs(mm) - 1;
+          for (uint64_t mm = passm; mm; mm &= mm - 1ull) {
+            const int e = __ffsll(mm) - 1;
             ib[pos & (kInbox - 1)] = word_of(elem_bits(e), e);
             ++pos;
           }
         }
-#if TOPK_TIMELINE
+#if TL_CYCLES
         __syncwarp();
         if (tl0) TL_ACC(tlc, kCycCandWrite, cres);
 #endif
@@ -1781,24 +1828,25 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[stage]);
-        if (warp == 0) *reinterpret_cast<volatile uint32_t*>(&st.fprog) = ++released;
+        // (the selectors' pre-final compares this with global stage indices)
+        if (warp == 0) *reinterpret_cast<volatile uint32_t*>(&st.fprog) = gs + 1u;
       }
       if (tl0) TL_ACC(tlc, kCycFiltBody, cbody);
-      if (tl0 && (d.tag & kLast)) TL_PIECE(tl_piece, 2);
-      if (d.tag & kLast) {
-        __syncwarp();
+      if (tl0 && (d.tag & kLast)) TL_PIECE(seq, 2);
+      // every warp reports each stage it has finished (its words reserved):
+      // the selectors know how many stages a piece has
+      __syncwarp();
+      if (d.tag & kLastG) {
+        // the group's last stage of the piece: its admitted count
         admitted = __reduce_add_sync(0xFFFFFFFFu, admitted);
-        if (lane == 0) {
-          if (admitted) atomicAdd(&p.admitted[r], admitted);
-          __threadfence_block();
-          atomicAdd(&st.fdone[par], 1);
-        }
+        if (lane == 0 && admitted) atomicAdd(&p.admitted[r], admitted);
         admitted = 0;
       }
-      if (++stage == nstage) {
-        stage = 0;
-        phase ^= 1u;
+      if (lane == 0) {
+        __threadfence_block();
+        atomicAdd(&st.fdone[par], 1);
       }
+      gs += uint32_t(kFG);
     }
     saw_nan = __any_sync(0xFFFFFFFFu, saw_nan);
     timed_out = __any_sync(0xFFFFFFFFu, timed_out);
@@ -1827,6 +1875,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   uint32_t head = 0, head_other = 0;  // inbox heads: this piece's parity, the other one
   int par = 0;
   int warm_next = 0;  // next piece whose starting threshold is to be set
+  int fd_cum0 = 0, fd_cum1 = 0;  // filter completions expected so far, per inbox parity
   TL_CYC_DECL(tlc);   // (timeline: accumulated by selector thread 0)
 
   // Publish a threshold to the filters (and to the row's other CTAs).
@@ -2079,8 +2128,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       head = head_other;
       head_other = h;
     }
-    const int fd_target = kNF * (j / 2 + 1);
     const int pc_nu = pc.u_end - pc.u_begin;
+    // stage reports that make the piece done: every warp of a stage's group
+    // reports it (an empty row is one stage), added up per inbox parity
+    const int fd_add = kGW * max(pc_nu, 1);
+    if (par) fd_cum1 += fd_add;
+    else fd_cum0 += fd_add;
+    const int fd_target = par ? fd_cum1 : fd_cum0;
     const uint32_t pre_at = pc.g_first + uint32_t(pc_nu) - uint32_t(kPreFinal);
     bool pre_done = pc_nu < kPreFinalMin;
 

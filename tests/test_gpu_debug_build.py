@@ -132,9 +132,11 @@ def test_timeline_build_records_the_launch():
     t = table.astype(np.int64)[:s["ctas"]]
     start, setup, exit_ = t[:, 0], t[:, 1], t[:, 7]
     assert np.all(start > 0) and np.all(setup >= start) and np.all(exit_ >= setup)
-    # every CTA of the flat plan took at least one piece and streamed stages
+    # every CTA of the flat plan took at least one piece; its first piece's
+    # threshold came before the selectors finished it
     assert np.all((t[:, 8] >> 32) >= 1)
-    assert s["per_cta_mean"]["filt_stages"] > 0
+    theta0, done0 = t[:, TLM.PIECE0], t[:, TLM.PIECE0 + 3]
+    assert np.all(theta0 > 0) and np.all(done0 >= theta0)
     assert 0 < s["span_us"] < 10_000
     # the normal build has no table
     assert B.LIB.topk_timeline_read(np.zeros(4, np.uint64).ctypes.data, None) == B.TOPK_ERR_ARG
