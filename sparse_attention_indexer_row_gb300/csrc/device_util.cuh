@@ -98,6 +98,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch (sm_90+).  A grid launched with programmatic
+// stream serialization may start while the grid before it in the stream is
+// still running; grid_dep_wait() blocks the calling thread until that grid has
+// completed and its memory is visible, so every thread calls it before it
+// touches global memory another grid may write.  grid_dep_launch() lets the
+// next such grid be scheduled on SMs this one leaves free.
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // A team of NT threads that synchronises on named barrier BAR.
 
 template <int NT, int BAR>

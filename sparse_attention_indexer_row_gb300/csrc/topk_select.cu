@@ -1417,6 +1417,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   // held across every role would cost the selector loop a spill)
 #define wl (*reinterpret_cast<volatile uint32_t*>(&st.wait_limit))
   if (tid == 0) TL_SET(kTlStart, tl_now());
+  // The next grid in the stream may be scheduled on SMs this one leaves; it
+  // waits for this grid to complete before it reads global memory.
+  if (tid == 0) grid_dep_launch();
 
   for (int j = tid; j < kp; j += kThreads) kept[j] = 0ull;
   for (int j = tid; j < kInbox; j += kThreads) {
@@ -1455,6 +1458,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     const uint64_t l2pol = l2_policy_evict_first();
     bool gave_up = false;
     bool stalled = false;  // test only: the producer stopped for good
+    // Global memory (the plan's lengths and queue, the scores) only after the
+    // grid before this one has completed.  The flat plan's pieces and
+    // visiting orders are arithmetic: they are drawn before that wait.
+    bool dep_done = false;
+    auto dep_wait = [&]() {
+      if (!dep_done) {
+        grid_dep_wait();
+        dep_done = true;
+      }
+    };
+    if (p.plan != kPlanFlat) dep_wait();
     TL_CYC_DECL(tlc);
     uint32_t g = 0;  // stages issued (lane 0)
     int stage = 0;
@@ -1504,6 +1518,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (nu == 0 && lane == 0) {
         // an empty row still flows through the filters and selectors: one
         // stage with no elements
+        dep_wait();
         next_slot();
         StageDesc d;
         d.e0 = 0;
@@ -1546,6 +1561,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
               stalled = true;
               break;
             }
+            dep_wait();
             next_slot();
             const uint32_t u = uint32_t(pc.u_begin + c0) + (perm[i] & uint32_t(kPermChunk - 1));
             const uint32_t e0 = u * uint32_t(kUnit);
@@ -1600,6 +1616,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       ++seq;
       if (stalled) break;
     }
+    dep_wait();
     if (lane == 0) {
       TL_SET(kTlLastCopy, tl_now());
       *reinterpret_cast<volatile int*>(&st.npieces) = seq;
@@ -1637,6 +1654,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   // candidate path when some lane has a survivor) once for 2048 elements, and
   // the two groups' latencies overlap.
   if (warp < kNF) {
+    grid_dep_wait();  // (before any global access: see the producer)
     const int grp = warp / kGW;     // filter group
     const int tg = tid - grp * kGT;  // 0 .. kGT-1 within the group
     uint64_t th = 0ull;
@@ -1862,6 +1880,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
   }
 
   // ---------------- selector warps: a6, a7, a8 ----------------
+  grid_dep_wait();  // (before any global access: see the producer)
   const int stt = tid - kNFT;  // 0 .. kNST-1
   const int swarp = stt >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
@@ -2284,13 +2303,20 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     // through the split-row ticket)
     TL_CLK(cend);
     if (tray_n > 0) {
-      if (kept_n > 0 && tray_n <= kNST && kp >= kNST) {
-        // Only the last stages' words are left (the kept list holds the best
-        // kp of everything before): sort them and merge, no select needed.
-        for (int t = tray_n + stt; t < kNST; t += kNST) tray[t] = 0ull;
+      if (tray_n <= kp && kp >= kNST) {
+        // At most kp words are left (the kept list, if any, holds the best kp
+        // of everything before): sort them and merge them in, or take them
+        // as the list -- no select needed.
+        const int P = max(next_pow2_dev(tray_n), kNST);  // <= kp
+        for (int t = tray_n + stt; t < P; t += kNST) tray[t] = 0ull;
         Sel::sync();
-        team_sort_desc<Sel>(tray, kNST, 2, stt);
-        merge_into_kept<Sel>(kept, tray, kNST, kp, stt);
+        team_sort_desc<Sel>(tray, P, 2, stt);
+        if (kept_n > 0) {
+          merge_into_kept<Sel>(kept, tray, P, kp, stt);
+        } else {
+          for (int q = stt; q < kp; q += kNST) kept[q] = q < P ? tray[q] : 0ull;
+          Sel::sync();
+        }
         ++nsorts;
         nsorted += uint32_t(tray_n);
         kept_n = min(kp, kept_n + tray_n);
@@ -3155,8 +3181,21 @@ static int launch_select(const float* scores, int32_t rows, int64_t n, int64_t r
     if (cudaGetLastError() != cudaSuccess) return TOPK_ERR_LAUNCH;
     p.order = order;
   }
-  topk_select_kernel<<<unsigned(G), kThreads, smem_layout(kp).total,
-                       static_cast<cudaStream_t>(stream)>>>(p);
+  // Launched with programmatic stream serialization: the grid may start while
+  // the stream's previous grid finishes (its set-up and, for the flat plan, its
+  // plan and first visiting keys overlap that grid's tail); it reads global
+  // memory only after that grid has completed (griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(G));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = size_t(smem_layout(kp).total);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, topk_select_kernel, p) != cudaSuccess) return TOPK_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
 }
 
