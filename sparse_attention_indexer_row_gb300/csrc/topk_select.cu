@@ -145,8 +145,8 @@ constexpr uint64_t kDefaultSeed = 0x5EEDC0DE1234ABCDull;
 #define TOPK_TIMELINE 0
 #endif
 constexpr int kTlSlots = 128;  // u64 slots per CTA
-constexpr int kTlPieces = 8;   // pieces recorded per CTA
-constexpr int kTlPerPiece = 8; // slots per piece
+constexpr int kTlPieces = 4;    // pieces recorded per CTA
+constexpr int kTlPerPiece = 16; // slots per piece
 enum TlSlot : int {
   kTlStart = 0,       // kernel entry
   kTlSetup = 1,       // after the set-up barrier
@@ -163,13 +163,18 @@ enum TlSlot : int {
   kTlWarmUnit0 = 12,  // ... its first unit read and the warps' keys shared
   kTlWarmCount = 13,  // ... the sample counted
   kTlWarmSecond = 14, // ... a second round counted (if one ran)
-  kTlPiece0 = 16,     // per piece p: kTlPerPiece slots from kTlPiece0 + 8p:
+  kTlPiece0 = 16,     // per piece p: kTlPerPiece slots from kTlPiece0 + 16p:
                       //   +0 starting threshold published, +1 filter warp 0
-                      //   takes its first stage, +2 filter warp 0 releases its
-                      //   last stage, +3 selectors done with it (row written
-                      //   or partial list published; a leader after its merge),
-                      //   +4 final tray sort and merge done, +5 ticket taken,
-                      //   +6 leader: partner lists merged, +7 pre-final sort done
+                      //   takes its first stage, +2 filter group 0 (warp 0)
+                      //   releases its last stage, +3 selectors done with it
+                      //   (row written or partial list published; a leader
+                      //   after its merge), +4 final tray sort and merge done,
+                      //   +5 ticket taken, +6 leader: partner lists merged,
+                      //   +7 pre-final sort done, +8 selectors see the piece's
+                      //   filters done, +9 pre-final started, +10 final sort
+                      //   done (before its merge), +11 partial list published
+                      //   (before the ticket), +12 filter group 1 releases its
+                      //   last stage, +13 producer: last copy issued
   kTlCyc0 = kTlPiece0 + kTlPieces * kTlPerPiece,  // cycle accumulators, see TlCyc
 };
 enum TlCyc : int {
@@ -432,9 +437,10 @@ struct __align__(16) StageDesc {
   uint32_t e0;      // row-local index of the unit's first element
   uint32_t nvalid;  // valid elements in the unit (0 for an empty row)
   uint32_t r;       // row
-  uint32_t tag;     // piece sequence number | kFirst | kLast, or kEnd
+  uint32_t tag;     // piece sequence number | kSample | kFirst | kLast | kLastG, or kEnd
 };
-constexpr uint32_t kSeqMask = 0x0FFFFFFFu;
+constexpr uint32_t kSeqMask = 0x07FFFFFFu;
+constexpr uint32_t kSample = 1u << 27; // one of the units the piece's warm start reads
 constexpr uint32_t kFirst = 1u << 28;  // the piece's first stage
 constexpr uint32_t kLast = 1u << 29;   // the piece's last stage
 constexpr uint32_t kEnd = 1u << 30;    // no more stages
@@ -506,6 +512,9 @@ struct CtaState {
   unsigned long long spec[2];      // speculative threshold word of the piece using inbox p
   const uint64_t* gsrc[16];        // leader merge: the partial lists of one gather step
   int warm_pub;                    // pieces whose starting threshold is set
+  int warm_claim;                  // pieces whose starting threshold some role has taken on
+  int adopted[2];                  // 1 + the piece of parity p that adopted its row's words
+  uint32_t est6[kNS];              // warm start: per selector warp second largest key
   int first_issued;                // pieces whose first stage the producer has issued
   uint32_t fprog;                  // stages filter warp 0 has released
   int sel_pre;                     // selector step: pre-final due
@@ -542,6 +551,52 @@ __device__ __noinline__ uint32_t queue_take(uint32_t* queue, uint32_t total) {
     }
   }
   return __shfl_sync(0xFFFFFFFFu, q, 0);
+}
+
+// Piece w starts from its split row's shared words (rt proven, rs
+// speculative; at least one is set): the role that claimed the piece
+// publishes them as the piece's threshold.
+__device__ __forceinline__ void adopt_row_theta(CtaState& st, int w, unsigned long long rt,
+                                                unsigned long long rs) {
+  if (rt != 0ull) atomicMax(&st.theta[w & 1], rt);
+  if (rs > rt) {
+    atomicMax(&st.theta[w & 1], rs);
+    atomicMax(&st.spec[w & 1], rs);
+  }
+  // (no warm start reads its sample units: the filters release them alone)
+  *reinterpret_cast<volatile int*>(&st.adopted[w & 1]) = w + 1;
+  __threadfence_block();
+  atomicMax(&st.warm_pub, w + 1);
+  TL_PIECE(w, 0);
+}
+
+// A filter warp's lane 0 at the first stage of piece seq: wait (at most
+// `limit` polls) for the piece's starting threshold.  The selectors set it
+// once its first units have landed, and only after piece seq - 2 (which used
+// the same inbox, counters and threshold word) is finished.  A piece of a
+// split row whose other CTAs already share a threshold need not wait for the
+// selectors (they may still be finishing the piece before): once piece
+// seq - 2 is finished, the filter warp that claims the piece first adopts
+// the row's words itself.  Out of line: it runs once per piece.
+__device__ __noinline__ bool filter_wait_theta(const unsigned long long* row_theta,
+                                               const unsigned long long* row_spec, CtaState& st,
+                                               int seq, uint32_t limit) {
+  const Piece& pc = st.table[seq % kTable];
+  for (uint32_t it = 0; *reinterpret_cast<volatile int*>(&st.warm_pub) < seq + 1; ++it) {
+    if (it > limit) return false;
+    if (pc.contributors > 1 && (it & 3u) == 0u &&
+        *reinterpret_cast<volatile int*>(&st.sel_pieces) >= seq - 1 &&
+        *reinterpret_cast<volatile int*>(&st.warm_claim) == seq) {
+      const unsigned long long rt = *reinterpret_cast<const volatile unsigned long long*>(&row_theta[pc.r]);
+      const unsigned long long rs = *reinterpret_cast<const volatile unsigned long long*>(&row_spec[pc.r]);
+      if ((rt | rs) != 0ull && atomicCAS(&st.warm_claim, seq, seq + 1) == seq) {
+        adopt_row_theta(st, seq, rt, rs);
+        return true;
+      }
+    }
+    __nanosleep(200);
+  }
+  return true;
 }
 
 // The pi-th piece of this CTA: 0 = no more pieces, 1 = a piece, 2 = an
@@ -1033,6 +1088,15 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
     if (need64 <= (wu == kWarmUnits ? uint64_t(kSpecMaxNeed) : 128ull)) {
       const uint32_t need = uint32_t(need64);
       const int R = need <= 128u ? 1 : int((5u * need + 4u * wu * kNS - 1u) / (4u * wu * kNS));
+      // Early start (rows of at least 2000 k elements, a full first unit):
+      // the smallest of the selector warps' second largest keys of the first
+      // unit is published as a speculative threshold at once, so that the
+      // filters start while the sample is counted.  A warp's share is 1024
+      // elements; for the row's k-th word to lie above that bound every warp
+      // must hold two of the row's top k, each with probability at most
+      // about 0.09 at L >= 2000 k (Poisson mean 1024 k / L <= 0.512): about
+      // 10^-8 for the eight.  A miss costs a rescan, never a wrong result.
+      bool early = false;
       float lm = -__int_as_float(0x7F800000);
       uint32_t wkey = 0u;  // this warp's rank-R key of the first unit
       {
@@ -1040,15 +1104,29 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
         StageDesc d;
         uint32_t copied;
         stage_of(0, src, d, copied);
+        early = R == 1 && copied == uint32_t(kUnit) && uint64_t(pw.L) >= 2000ull * uint64_t(k);
         if (R > 1) {
           float x[kEPT];
           const uint32_t valid = load_share(x, src, wrow, d.e0, d.nvalid, copied, stt);
           wkey = warp_key_bound(x, valid, R, 1);  // exact: a coarse bound could pass a whole top unit
         } else if (copied == uint32_t(kUnit)) {
+          float lm2 = -__int_as_float(0x7F800000);  // the lane's second largest
 #pragma unroll
           for (int u = 0; u < kF4; ++u) {
             const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
-            lm = fmaxf(lm, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              lm2 = fmaxf(lm2, fminf(lm, vv[c]));
+              lm = fmaxf(lm, vv[c]);
+            }
+          }
+          if (early) {
+            const uint32_t a1 = Top4::key_of(lm), a2 = Top4::key_of(lm2);
+            const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, a1);
+            const uint32_t at_top = __ballot_sync(0xFFFFFFFFu, a1 == m1);
+            const uint32_t m2 = __popc(at_top) > 1 ? m1 : __reduce_max_sync(0xFFFFFFFFu, a1 == m1 ? a2 : a1);
+            if (lane == 0) st.est6[swarp] = m2;
           }
         } else {
           for (int u = 0; u < kF4; ++u) {
@@ -1072,6 +1150,20 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
       }
       Sel::sync();
       if (stt == 0 && w == 0) TL_SET(kTlWarmUnit0, tl_now());
+      if (early && stt == 0) {
+        uint32_t e = 0xFFFFFFFFu;
+#pragma unroll
+        for (int q = 0; q < kNS; ++q) e = min(e, st.est6[q]);
+        if (e > 1u) {
+          const uint64_t se = (uint64_t(e) << 32) - 1ull;
+          if (pw.contributors > 1) atomicMax(&row_spec[pw.r], (unsigned long long)se);
+          atomicMax(&st.theta[w & 1], (unsigned long long)se);
+          if (se > st.spec[w & 1]) st.spec[w & 1] = se;
+          __threadfence_block();
+          atomicMax(&st.warm_pub, w + 1);
+          TL_PIECE(w, 0);
+        }
+      }
       // the three smallest warp maxima
       uint32_t s8 = 0xFFFFFFFFu, s7 = 0xFFFFFFFFu, s6 = 0xFFFFFFFFu;
 #pragma unroll
@@ -1322,13 +1414,19 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
     if (spec > th0) {
       if (pw.contributors > 1) atomicMax(&row_spec[pw.r], (unsigned long long)spec);
       atomicMax(&st.theta[w & 1], (unsigned long long)spec);
-      st.spec[w & 1] = spec;
+      if (spec > st.spec[w & 1]) st.spec[w & 1] = spec;
     }
     __threadfence_block();
-    *reinterpret_cast<volatile int*>(&st.warm_pub) = w + 1;
+    atomicMax(&st.warm_pub, w + 1);
     TL_PIECE(w, 0);
   }
   Sel::sync();  // the bounds are read before the next warm start rewrites them
+  // every read of the sample units is done: their own arrivals (the producer
+  // may reuse their slots once the filters have released them too)
+  if (stt == 0) {
+    uint64_t* empty = full + nstage;
+    for (int q = 0; q < wu; ++q) mbar_arrive(&empty[(pw.g_first + uint32_t(q)) % uint32_t(nstage)]);
+  }
   return ok;
 #undef wl
 }
@@ -1438,13 +1536,22 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     st.pieces_pub = 0;
     st.npieces = -1;
     st.warm_pub = 0;
+    st.warm_claim = 0;
+    st.adopted[0] = 0;
+    st.adopted[1] = 0;
     st.first_issued = 0;
     st.fprog = 0u;
     st.flags = 0;
     st.wait_limit = p.wait_limit;
     for (int i = 0; i < nstage; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kGW);  // the warps of the stage's filter group
+      // the warps of the stage's filter group, plus one arrival for the unit:
+      // the producer's when it issues the copy, or, for a warm-start unit,
+      // the warm start's once it no longer reads it (a piece's filters may
+      // start from an early threshold while its warm start still counts the
+      // sample; a piece that adopts its row's words has no warm start, and
+      // its filters' first group warp arrives twice)
+      mbar_init(&empty[i], kGW + 1);
     }
     mbar_init_fence();
   }
@@ -1524,7 +1631,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         d.e0 = 0;
         d.nvalid = 0;
         d.r = uint32_t(pc.r);
-        d.tag = uint32_t(seq) | kFirst | kLast | kLastG;
+        d.tag = uint32_t(seq) | kSample | kFirst | kLast | kLastG;
         desc[stage] = d;
         mbar_arrive(&full[stage]);
         *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
@@ -1571,7 +1678,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             d.e0 = e0;
             d.nvalid = nvalid;
             d.r = uint32_t(pc.r);
-            d.tag = uint32_t(seq) | (c0 == 0 && i == 0 ? kFirst : 0u) |
+            d.tag = uint32_t(seq) | (c0 == 0 && i < wu ? kSample : 0u) | (c0 == 0 && i == 0 ? kFirst : 0u) |
                     (c0 + i == nu - 1 ? kLast : 0u) | (c0 + i >= nu - 2 ? kLastG : 0u);
             desc[stage] = d;
             fence_proxy_async_smem();
@@ -1581,11 +1688,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             } else {
               mbar_arrive(&full[stage]);
             }
+            if (!(c0 == 0 && i < wu)) mbar_arrive(&empty[stage]);
             if (g == 0u) TL_SET(kTlFirstCopy, tl_now());
             // Until a piece's first wu stages are issued, their ring slots'
             // barriers may still be in an earlier phase: the selectors look at
             // them only after this count says the stages are on their way.
             if (c0 + i == wu - 1) *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
+            if (c0 + i == nu - 1) TL_PIECE(seq, 13);
             advance();
           }
         };
@@ -1687,23 +1796,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       if (d.tag & kEnd) break;
       const int seq = int(d.tag & kSeqMask);
       if (seq != cur_seq) {
-        // The group's first stage of a piece.  The selectors set the piece's
-        // starting threshold once its first units have landed, and only after
-        // piece seq - 2 (which used the same inbox, counters and threshold
-        // word) is finished.
+        // The group's first stage of a piece: wait for its starting
+        // threshold (see filter_wait_theta).
         cur_seq = seq;
         par = seq & 1;
         TL_CLK(ct);
-        if (lane == 0) {
-          uint32_t it = 0;
-          while (*reinterpret_cast<volatile int*>(&st.warm_pub) < seq + 1) {
-            if (++it > wl) {
-              timed_out = true;
-              break;
-            }
-            __nanosleep(200);
-          }
-        }
+        if (lane == 0 && !filter_wait_theta(p.row_theta, p.row_spec, st, seq, wl)) timed_out = true;
         if (__any_sync(0xFFFFFFFFu, timed_out)) {
           timed_out = true;
           break;
@@ -1846,11 +1944,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[stage]);
+        if ((d.tag & kSample) && warp % kGW == 0 &&
+            *reinterpret_cast<volatile int*>(&st.adopted[par]) == seq + 1)
+          mbar_arrive(&empty[stage]);  // (the unit's own arrival: no warm start reads it)
         // (the selectors' pre-final compares this with global stage indices)
         if (warp == 0) *reinterpret_cast<volatile uint32_t*>(&st.fprog) = gs + 1u;
       }
       if (tl0) TL_ACC(tlc, kCycFiltBody, cbody);
-      if (tl0 && (d.tag & kLast)) TL_PIECE(seq, 2);
+      if (lane == 0 && (d.tag & kLastG) && (tid == 0 || tid == kGT)) TL_PIECE(seq, tid == 0 ? 2 : 12);
       // every warp reports each stage it has finished (its words reserved):
       // the selectors know how many stages a piece has
       __syncwarp();
@@ -2170,8 +2271,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
           // starting threshold.  A split row whose other CTAs have already
           // published a threshold starts from that one at once (action 2);
           // otherwise the warm start runs once its units have landed
-          // (action 1).
+          // (action 1).  Either is claimed first: the filters may already
+          // have taken the piece on (they adopt a split row's shared
+          // threshold when they reach the piece first): then it is skipped
+          // (action 3).
           bool warm_due = false;
+          if (warm_next <= j + 1 && *reinterpret_cast<volatile int*>(&st.warm_claim) > warm_next) {
+            warm = 3;
+            break;
+          }
           if (warm_next <= j + 1 && *reinterpret_cast<volatile int*>(&st.pieces_pub) > warm_next) {
             const Piece& pn = st.table[warm_next % kTable];
             const unsigned long long rt =
@@ -2185,15 +2293,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
                     ? *reinterpret_cast<volatile unsigned long long*>(&p.row_spec[pn.r])
                     : 0ull;
             if (rt != 0ull || rs != 0ull) {
-              if (rt != 0ull) atomicMax(&st.theta[warm_next & 1], rt);
-              if (rs > rt) {
-                atomicMax(&st.theta[warm_next & 1], rs);
-                st.spec[warm_next & 1] = rs;
+              warm = 3;
+              if (atomicCAS(&st.warm_claim, warm_next, warm_next + 1) == warm_next) {
+                adopt_row_theta(st, warm_next, rt, rs);
+                warm = 2;
               }
-              __threadfence_block();
-              *reinterpret_cast<volatile int*>(&st.warm_pub) = warm_next + 1;
-              TL_PIECE(warm_next, 0);
-              warm = 2;
               break;
             }
             if (*reinterpret_cast<volatile int*>(&st.first_issued) > warm_next) {
@@ -2212,7 +2316,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
                 landed = mbar_try_wait(&full[g % uint32_t(nstage)], (g / uint32_t(nstage)) & 1u);
               }
               if (landed) {
-                warm = 1;
+                warm = atomicCAS(&st.warm_claim, warm_next, warm_next + 1) == warm_next ? 1 : 3;
                 break;
               }
               warm_due = true;  // issued, not landed yet
@@ -2276,6 +2380,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       }
       if (pre) {
         pre_done = true;
+        if (stt == 0) TL_PIECE(j, 9);
         TL_CLK(ct);
         if (n > 0) take(n);
         if (stt == 0) TL_ACC(tlc, kCycSelTake, ct);
@@ -2302,6 +2407,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     // end of the piece: final sort, then the row's output (directly, or
     // through the split-row ticket)
     TL_CLK(cend);
+    if (stt == 0) TL_PIECE(j, 8);
     if (tray_n > 0) {
       if (tray_n <= kp && kp >= kNST) {
         // At most kp words are left (the kept list, if any, holds the best kp
@@ -2311,6 +2417,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         for (int t = tray_n + stt; t < P; t += kNST) tray[t] = 0ull;
         Sel::sync();
         team_sort_desc<Sel>(tray, P, 2, stt);
+        if (stt == 0) TL_PIECE(j, 10);
         if (kept_n > 0) {
           merge_into_kept<Sel>(kept, tray, P, kp, stt);
         } else {
@@ -2352,6 +2459,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       __threadfence();
       Sel::sync();
       if (stt == 0) {
+        TL_PIECE(j, 11);
         const uint32_t t = atomicAdd(&p.tickets[pc.r], 1u);
         st.leader = (t == uint32_t(pc.contributors - 1)) ? 1 : 0;
         TL_PIECE(j, 5);

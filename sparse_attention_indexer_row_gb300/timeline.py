@@ -25,17 +25,20 @@ SLOT = {"start": 0, "setup": 1, "first_copy": 2, "last_copy": 3, "prod_exit": 4,
         "prod_order": 10, "warm_enter": 11, "warm_unit0": 12, "warm_count": 13,
         "warm_second": 14}
 PIECE0 = 16
-PIECES = 8
-PER_PIECE = 8
+PIECES = 4
+PER_PIECE = 16
 CYC0 = PIECE0 + PIECES * PER_PIECE
 CYC = ["filt_wait_full", "filt_wait_theta", "filt_cand", "filt_stages", "filt_cand_stages",
        "sel_warm", "sel_take", "sel_prune", "sel_sort", "sel_end", "sel_poll", "sel_leaders",
        "prod_wait_empty", "sel_rescans", "filt_body", "cand_classify", "cand_reserve",
        "cand_write", "cand_words", "filt_load"]
 COUNTS = {"filt_stages", "filt_cand_stages", "sel_leaders", "sel_rescans", "cand_words"}
-# per-piece events: +0 threshold published, +1 filters' first stage, +2 filters'
-# last release, +3 selectors done, +4 final sort done, +5 ticket taken,
-# +6 leader's merge done, +7 pre-final sort done
+# per-piece events: +0 threshold published, +1 filters' first stage, +2 filter
+# group 0's last release, +3 selectors done, +4 final sort and merge done,
+# +5 ticket taken, +6 leader's merge done, +7 pre-final sort done, +8 selectors
+# see the filters done, +9 pre-final started, +10 final sort done (before its
+# merge), +11 partial list published, +12 filter group 1's last release,
+# +13 producer's last copy of the piece
 
 
 def load():
@@ -96,7 +99,8 @@ def summarize(table: np.ndarray, sm_mhz: float) -> dict:
     lag = {"prefinal_before_last": [], "final": [], "ticket": [], "leader": [], "done": []}
     for p in range(PIECES):
         base = PIECE0 + PER_PIECE * p
-        th, ff, fl, sd, fs, tk, ld, pf = (t[:, base + i] for i in range(8))
+        th, ff, fl0, sd, fs, tk, ld, pf = (t[:, base + i] for i in range(8))
+        fl = np.maximum(fl0, t[:, base + 12])  # both filter groups' last releases
         ok = (fl > 0) & (pf > 0)
         lag["prefinal_before_last"].extend(((fl[ok] - pf[ok]) / 1e3).tolist())
         if p == 0:
