@@ -437,10 +437,9 @@ struct __align__(16) StageDesc {
   uint32_t e0;      // row-local index of the unit's first element
   uint32_t nvalid;  // valid elements in the unit (0 for an empty row)
   uint32_t r;       // row
-  uint32_t tag;     // piece sequence number | kSample | kFirst | kLast | kLastG, or kEnd
+  uint32_t tag;     // piece sequence number | kFirst | kLast | kLastG, or kEnd
 };
-constexpr uint32_t kSeqMask = 0x07FFFFFFu;
-constexpr uint32_t kSample = 1u << 27; // one of the units the piece's warm start reads
+constexpr uint32_t kSeqMask = 0x0FFFFFFFu;
 constexpr uint32_t kFirst = 1u << 28;  // the piece's first stage
 constexpr uint32_t kLast = 1u << 29;   // the piece's last stage
 constexpr uint32_t kEnd = 1u << 30;    // no more stages
@@ -513,8 +512,6 @@ struct CtaState {
   const uint64_t* gsrc[16];        // leader merge: the partial lists of one gather step
   int warm_pub;                    // pieces whose starting threshold is set
   int warm_claim;                  // pieces whose starting threshold some role has taken on
-  int adopted[2];                  // 1 + the piece of parity p that adopted its row's words
-  uint32_t est6[kNS];              // warm start: per selector warp second largest key
   int first_issued;                // pieces whose first stage the producer has issued
   uint32_t fprog;                  // stages filter warp 0 has released
   int sel_pre;                     // selector step: pre-final due
@@ -563,8 +560,6 @@ __device__ __forceinline__ void adopt_row_theta(CtaState& st, int w, unsigned lo
     atomicMax(&st.theta[w & 1], rs);
     atomicMax(&st.spec[w & 1], rs);
   }
-  // (no warm start reads its sample units: the filters release them alone)
-  *reinterpret_cast<volatile int*>(&st.adopted[w & 1]) = w + 1;
   __threadfence_block();
   atomicMax(&st.warm_pub, w + 1);
   TL_PIECE(w, 0);
@@ -979,6 +974,33 @@ struct Top4 {
   }
 };
 
+// The warp's exact R-th largest key over its elements (as warp_key_bound
+// with low = 1: the largest T that at least R keys reach; 0 if fewer than R
+// are valid), for a small R: the warp takes its largest key value below the
+// last one taken, R times at most, counting the elements equal to it, until
+// R elements have been taken -- R rounds of one pass instead of sixteen
+// bisection rounds.
+__device__ __forceinline__ uint32_t warp_rank_key(const float (&x)[kEPT], uint32_t valid, int R) {
+  uint32_t key[kEPT];
+#pragma unroll
+  for (int e = 0; e < kEPT; ++e) key[e] = share_key(x, valid, e);
+  uint32_t taken = 0, prev = 0xFFFFFFFFu;  // (no key is all ones: +inf's is 0xFF800000)
+  for (int it = 0; it < R; ++it) {
+    uint32_t lm = 0u;
+#pragma unroll
+    for (int e = 0; e < kEPT; ++e) lm = max(lm, key[e] < prev ? key[e] : 0u);
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, lm);
+    if (m == 0u) return 0u;  // fewer than R valid elements
+    uint32_t c = 0u;
+#pragma unroll
+    for (int e = 0; e < kEPT; ++e) c += key[e] == m ? 1u : 0u;
+    taken += __reduce_add_sync(0xFFFFFFFFu, c);
+    if (taken >= uint32_t(R)) return m;
+    prev = m;
+  }
+  return 0u;  // (not reached: every round takes at least one element)
+}
+
 // For m > 64 the counts run over all 32 keys of each lane (one unit).  The
 // bound resolves the key down to bit `low` (17: a 16-bit prefix; 1: the exact
 // m-th key).
@@ -1088,15 +1110,6 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
     if (need64 <= (wu == kWarmUnits ? uint64_t(kSpecMaxNeed) : 128ull)) {
       const uint32_t need = uint32_t(need64);
       const int R = need <= 128u ? 1 : int((5u * need + 4u * wu * kNS - 1u) / (4u * wu * kNS));
-      // Early start (rows of at least 2000 k elements, a full first unit):
-      // the smallest of the selector warps' second largest keys of the first
-      // unit is published as a speculative threshold at once, so that the
-      // filters start while the sample is counted.  A warp's share is 1024
-      // elements; for the row's k-th word to lie above that bound every warp
-      // must hold two of the row's top k, each with probability at most
-      // about 0.09 at L >= 2000 k (Poisson mean 1024 k / L <= 0.512): about
-      // 10^-8 for the eight.  A miss costs a rescan, never a wrong result.
-      bool early = false;
       float lm = -__int_as_float(0x7F800000);
       uint32_t wkey = 0u;  // this warp's rank-R key of the first unit
       {
@@ -1104,29 +1117,15 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
         StageDesc d;
         uint32_t copied;
         stage_of(0, src, d, copied);
-        early = R == 1 && copied == uint32_t(kUnit) && uint64_t(pw.L) >= 2000ull * uint64_t(k);
         if (R > 1) {
           float x[kEPT];
           const uint32_t valid = load_share(x, src, wrow, d.e0, d.nvalid, copied, stt);
-          wkey = warp_key_bound(x, valid, R, 1);  // exact: a coarse bound could pass a whole top unit
+          wkey = warp_rank_key(x, valid, R);  // exact: a coarse bound could pass a whole top unit
         } else if (copied == uint32_t(kUnit)) {
-          float lm2 = -__int_as_float(0x7F800000);  // the lane's second largest
 #pragma unroll
           for (int u = 0; u < kF4; ++u) {
             const float4 v = reinterpret_cast<const float4*>(src)[stt + kNST * u];
-            const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              lm2 = fmaxf(lm2, fminf(lm, vv[c]));
-              lm = fmaxf(lm, vv[c]);
-            }
-          }
-          if (early) {
-            const uint32_t a1 = Top4::key_of(lm), a2 = Top4::key_of(lm2);
-            const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, a1);
-            const uint32_t at_top = __ballot_sync(0xFFFFFFFFu, a1 == m1);
-            const uint32_t m2 = __popc(at_top) > 1 ? m1 : __reduce_max_sync(0xFFFFFFFFu, a1 == m1 ? a2 : a1);
-            if (lane == 0) st.est6[swarp] = m2;
+            lm = fmaxf(lm, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
           }
         } else {
           for (int u = 0; u < kF4; ++u) {
@@ -1150,20 +1149,6 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
       }
       Sel::sync();
       if (stt == 0 && w == 0) TL_SET(kTlWarmUnit0, tl_now());
-      if (early && stt == 0) {
-        uint32_t e = 0xFFFFFFFFu;
-#pragma unroll
-        for (int q = 0; q < kNS; ++q) e = min(e, st.est6[q]);
-        if (e > 1u) {
-          const uint64_t se = (uint64_t(e) << 32) - 1ull;
-          if (pw.contributors > 1) atomicMax(&row_spec[pw.r], (unsigned long long)se);
-          atomicMax(&st.theta[w & 1], (unsigned long long)se);
-          if (se > st.spec[w & 1]) st.spec[w & 1] = se;
-          __threadfence_block();
-          atomicMax(&st.warm_pub, w + 1);
-          TL_PIECE(w, 0);
-        }
-      }
       // the three smallest warp maxima
       uint32_t s8 = 0xFFFFFFFFu, s7 = 0xFFFFFFFFu, s6 = 0xFFFFFFFFu;
 #pragma unroll
@@ -1421,12 +1406,6 @@ __device__ __noinline__ bool warm_start_piece(const float* scores, int64_t row_s
     TL_PIECE(w, 0);
   }
   Sel::sync();  // the bounds are read before the next warm start rewrites them
-  // every read of the sample units is done: their own arrivals (the producer
-  // may reuse their slots once the filters have released them too)
-  if (stt == 0) {
-    uint64_t* empty = full + nstage;
-    for (int q = 0; q < wu; ++q) mbar_arrive(&empty[(pw.g_first + uint32_t(q)) % uint32_t(nstage)]);
-  }
   return ok;
 #undef wl
 }
@@ -1537,21 +1516,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
     st.npieces = -1;
     st.warm_pub = 0;
     st.warm_claim = 0;
-    st.adopted[0] = 0;
-    st.adopted[1] = 0;
     st.first_issued = 0;
     st.fprog = 0u;
     st.flags = 0;
     st.wait_limit = p.wait_limit;
     for (int i = 0; i < nstage; ++i) {
       mbar_init(&full[i], 1);
-      // the warps of the stage's filter group, plus one arrival for the unit:
-      // the producer's when it issues the copy, or, for a warm-start unit,
-      // the warm start's once it no longer reads it (a piece's filters may
-      // start from an early threshold while its warm start still counts the
-      // sample; a piece that adopts its row's words has no warm start, and
-      // its filters' first group warp arrives twice)
-      mbar_init(&empty[i], kGW + 1);
+      mbar_init(&empty[i], kGW);  // the warps of the stage's filter group
     }
     mbar_init_fence();
   }
@@ -1631,7 +1602,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
         d.e0 = 0;
         d.nvalid = 0;
         d.r = uint32_t(pc.r);
-        d.tag = uint32_t(seq) | kSample | kFirst | kLast | kLastG;
+        d.tag = uint32_t(seq) | kFirst | kLast | kLastG;
         desc[stage] = d;
         mbar_arrive(&full[stage]);
         *reinterpret_cast<volatile int*>(&st.first_issued) = seq + 1;
@@ -1678,7 +1649,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             d.e0 = e0;
             d.nvalid = nvalid;
             d.r = uint32_t(pc.r);
-            d.tag = uint32_t(seq) | (c0 == 0 && i < wu ? kSample : 0u) | (c0 == 0 && i == 0 ? kFirst : 0u) |
+            d.tag = uint32_t(seq) | (c0 == 0 && i == 0 ? kFirst : 0u) |
                     (c0 + i == nu - 1 ? kLast : 0u) | (c0 + i >= nu - 2 ? kLastG : 0u);
             desc[stage] = d;
             fence_proxy_async_smem();
@@ -1688,7 +1659,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
             } else {
               mbar_arrive(&full[stage]);
             }
-            if (!(c0 == 0 && i < wu)) mbar_arrive(&empty[stage]);
             if (g == 0u) TL_SET(kTlFirstCopy, tl_now());
             // Until a piece's first wu stages are issued, their ring slots'
             // barriers may still be in an earlier phase: the selectors look at
@@ -1944,9 +1914,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(const Params p
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[stage]);
-        if ((d.tag & kSample) && warp % kGW == 0 &&
-            *reinterpret_cast<volatile int*>(&st.adopted[par]) == seq + 1)
-          mbar_arrive(&empty[stage]);  // (the unit's own arrival: no warm start reads it)
         // (the selectors' pre-final compares this with global stage indices)
         if (warp == 0) *reinterpret_cast<volatile uint32_t*>(&st.fprog) = gs + 1u;
       }
