@@ -202,6 +202,15 @@ enum TlCyc : int {
 };
 static_assert(kTlPiece0 + kTlPerPiece * kTlPieces <= kTlCyc0 && kTlCyc0 + kCycCount <= kTlSlots,
               "timeline slots");
+// The short-row kernel's slots (its CTA's thread 0, SM cycles summed over the
+// CTA's rows): rows, row start (queue item, row order and length, first
+// loads issued), chunk loop without its selects, selects, row end (final
+// select, sort, write), whole CTA, chunks, selects, waits for a chunk to land.
+enum TlShort : int {
+  kTlShortRows = 100, kTlShortMeta, kTlShortChunks, kTlShortSelect, kTlShortEnd, kTlShortTotal,
+  kTlShortNChunks, kTlShortNSelects, kTlShortWait, kTlShortEndSlot
+};
+static_assert(kTlCyc0 + kCycCount <= kTlShortRows && kTlShortEndSlot <= kTlSlots, "timeline slots");
 
 #if TOPK_TIMELINE
 constexpr int kTlCtas = 512;   // CTAs recorded
@@ -2593,6 +2602,24 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
     const float* bmax, int64_t bstride, const int32_t* lengths, int64_t n, int32_t pool_blocks,
     int32_t pinned, int32_t* out_pool, uint32_t* status);
 
+// The short-row kernel (defined below) and its launch shape.
+constexpr int kShortThreads = 256;
+constexpr int kShortChunk = kShortThreads * 16;  // elements a chunk (16 KB: one bulk copy)
+constexpr int kShortStages = 2;                  // chunk copies in flight per CTA
+constexpr int kShortMaxN = 65536;                // longest row (valid length) of the path
+constexpr int kShortCtasPerSm = 3;               // resident CTAs per SM at most
+using Blk = Team<kShortThreads, 0>;              // (barrier 0 over the whole CTA)
+
+// tray mark (words before a select) and capacity for kept-list size kp; the
+// dynamic shared memory: tray, ring of chunk stages, their barriers
+__host__ __device__ inline int short_mark(int kp) { return kp <= 512 ? 1024 : 2 * kp; }
+__host__ __device__ inline int short_cap(int kp) { return short_mark(kp) + kShortChunk; }
+__host__ __device__ inline int short_smem(int kp) {
+  return short_cap(kp) * int(sizeof(uint64_t)) + kShortStages * kShortChunk * int(sizeof(float)) +
+         kShortStages * int(sizeof(uint64_t));
+}
+__global__ void __launch_bounds__(kShortThreads, kShortCtasPerSm) short_select_kernel(const Params p);
+
 cudaError_t configure_device(int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -2608,6 +2635,9 @@ cudaError_t configure_device(int* sms) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(pool_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kPoolSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(short_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           short_smem(TOPK_MAX_K));
   if (e != cudaSuccess) return e;
   int count = 0;
   e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
@@ -3074,6 +3104,291 @@ __global__ void __launch_bounds__(kPoolSelThreads) queue_order_kernel(
   for (int32_t r = t; r < rows; r += kPoolSelThreads) order[atomicAdd(&cnt[bin(r)], 1u)] = r;
 }
 
+// ---------------------------------------------------------------------------
+// Short rows (batches of many rows of at most kShortMaxN elements, the
+// prefill's causal rows): the same method -- a threshold that only rises, a
+// tray of the words above it, a select that raises it when the tray passes
+// its mark, a bitonic sort of the survivors at the end -- run by one 256-
+// thread CTA per row with no role split, several CTAs per SM, rows taken
+// from the shared queue (longest first).  A row of a few units would spend
+// most of the selection kernel's per-piece work (warm start, two-inbox
+// hand-over, piece end) waiting for its selector team; here a row is read in
+// 4096-element chunks (sixteen scores a thread, the next chunk's loads in
+// flight while this one is tested), and its first chunk sets the threshold.
+
+struct ShortState {
+  uint32_t hist[256];
+  int cnt;        // tray words (append counter)
+  int row;        // the queue item this CTA works on
+  int sel_b, sel_above, sel_binc;
+};
+
+// The exact best-k prefix of the tray's n words (all distinct, n > k): a
+// byte-wise radix select from the top byte finds a prefix T such that exactly
+// k words are >= T; those k words are compacted to the tray's front (a word
+// only moves down, and each round reads all its words before any is written).
+// Returns T.  Ends with a barrier.
+__device__ uint64_t short_select(uint64_t* tray, int n, int k, ShortState& st, int t,
+                                 uint32_t* status) {
+  const int lane = t & 31, warp = t >> 5;
+  uint64_t prefix = 0ull;
+  uint32_t need = uint32_t(k);
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    const uint64_t hmask = pass == 0 ? 0ull : (~0ull << (shift + 8));
+    for (int b = t; b < 256; b += kShortThreads) st.hist[b] = 0u;
+    Blk::sync();
+    for (int j = t; j < n; j += kShortThreads) {
+      const uint64_t w = tray[j];
+      if ((w & hmask) == prefix) atomicAdd(&st.hist[uint32_t(w >> shift) & 0xFFu], 1u);
+    }
+    Blk::sync();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 248-8l, scanned from the top
+      uint32_t c8[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        c8[q] = st.hist[255 - 8 * lane - q];
+        sum += c8[q];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += o;
+      }
+      const uint32_t excl = incl - sum;
+      if (excl < need && incl >= need) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (acc < need && acc + c8[q] >= need) {
+            st.sel_b = 255 - 8 * lane - q;
+            st.sel_above = int(acc);
+            st.sel_binc = int(c8[q]);
+          }
+          acc += c8[q];
+        }
+      }
+    }
+    Blk::sync();
+    const uint32_t b = uint32_t(st.sel_b), above = uint32_t(st.sel_above),
+                   binc = uint32_t(st.sel_binc);
+    prefix |= uint64_t(b) << shift;
+    need -= above;
+    if (binc == need) break;  // the whole bin is in: exactly k words are >= prefix
+  }
+  const uint64_t T = prefix;
+  if (t == 0) st.cnt = 0;
+  Blk::sync();
+  constexpr int R = 8;
+  for (int base0 = 0; base0 < n; base0 += R * kShortThreads) {
+    uint64_t w[R];
+    bool keep[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      const int j = base0 + u * kShortThreads + t;
+      w[u] = j < n ? tray[j] : 0ull;
+      keep[u] = j < n && w[u] >= T;
+    }
+    Blk::sync();
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, keep[u]);
+      if (mask) {
+        int at = 0;
+        if (lane == 0) at = atomicAdd(&st.cnt, __popc(mask));
+        at = __shfl_sync(0xFFFFFFFFu, at, 0);
+        const int pos = at + __popc(mask & ((1u << lane) - 1u));
+        if (keep[u] && IN_BOUNDS(pos < n, status)) tray[pos] = w[u];
+      }
+    }
+  }
+  Blk::sync();
+  return T;
+}
+
+__global__ void __launch_bounds__(kShortThreads, kShortCtasPerSm) short_select_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem_s[];
+  const int k = p.k, kp = p.kp;
+  const int mark = short_mark(kp), cap = short_cap(kp);
+  uint64_t* tray = reinterpret_cast<uint64_t*>(smem_s);
+  float* ring = reinterpret_cast<float*>(smem_s + size_t(cap) * sizeof(uint64_t));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kShortStages * kShortChunk);
+  __shared__ ShortState st;
+  const int t = threadIdx.x, lane = t & 31;
+  if (t == 0) {
+    grid_dep_launch();
+    for (int q = 0; q < kShortStages; ++q) mbar_init(&full[q], 1);
+    mbar_init_fence();
+  }
+  Blk::sync();
+  grid_dep_wait();  // (global memory only after the stream's previous grid)
+  const uint32_t total = uint32_t(p.rows);
+  const uint64_t l2pol = l2_policy_evict_first();
+  bool saw_nan = false, timed_out = false;
+  uint32_t g_issue = 0, g_use = 0;  // chunks issued (thread 0) and consumed, over the CTA's rows
+#if TOPK_TIMELINE
+  // (thread 0's cycle sums, see TlShort)
+  unsigned long long tls[kTlShortEndSlot - kTlShortRows] = {};
+  const long long tl_c0 = clock64();
+  long long tl_a = tl_c0;
+#define TLS_MARK(slot)                                      \
+  do {                                                      \
+    const long long tl_b = clock64();                       \
+    tls[(slot) - kTlShortRows] += (unsigned long long)(tl_b - tl_a); \
+    tl_a = tl_b;                                            \
+  } while (0)
+#define TLS_COUNT(slot, v) (tls[(slot) - kTlShortRows] += (unsigned long long)(v))
+#else
+#define TLS_MARK(slot) ((void)0)
+#define TLS_COUNT(slot, v) ((void)0)
+#endif
+  for (;;) {
+    if (t < 32) {
+      const uint32_t q = queue_take(p.queue, total);
+      if (t == 0) st.row = int(q);
+    }
+    if (t == 0) st.cnt = 0;
+    Blk::sync();
+    const uint32_t item = uint32_t(st.row);
+    if (item >= total) break;
+    const int32_t r = p.order ? p.order[item] : int32_t(item);
+    int64_t L = p.lengths ? int64_t(p.lengths[r]) : p.n;
+    if (L < 0 || L > p.n) {
+      if (t == 0) atomicOr(p.status, TOPK_STATUS_BAD_LENGTH);
+      L = L < 0 ? 0 : p.n;
+    }
+    const uint32_t Lu = uint32_t(L);
+    const uint32_t nc = (Lu + uint32_t(kShortChunk) - 1) / uint32_t(kShortChunk);
+    const float* row = p.scores + int64_t(r) * p.row_stride;
+    const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    // elements of chunk c in its stage (a 16-byte multiple; the rest, past
+    // it, come from global memory)
+    auto copied_of = [&](uint32_t c) -> uint32_t {
+      const uint32_t left = Lu - c * uint32_t(kShortChunk);
+      return aligned ? (min(left, uint32_t(kShortChunk)) & ~3u) : 0u;
+    };
+    // thread 0: chunk c of this row into the next stage
+    auto issue = [&](uint32_t c) {
+      const int stage = int(g_issue % uint32_t(kShortStages));
+      const uint32_t bytes = copied_of(c) * 4u;
+      fence_proxy_async_smem();
+      if (bytes) {
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        bulk_load_hint(ring + stage * kShortChunk, row + size_t(c) * kShortChunk, bytes,
+                       &full[stage], l2pol);
+      } else {
+        mbar_arrive(&full[stage]);
+      }
+      ++g_issue;
+    };
+    uint64_t theta = 0ull;  // words above it are admitted (0: every real word)
+    int tray_n = 0;
+    uint32_t admitted = 0;
+    TLS_MARK(kTlShortMeta);
+    TLS_COUNT(kTlShortRows, 1);
+    {
+      if (t == 0)
+        for (uint32_t c = 0; c < nc && c < uint32_t(kShortStages); ++c) issue(c);
+      for (uint32_t c = 0; c < nc; ++c) {
+        TLS_COUNT(kTlShortNChunks, 1);
+        const uint32_t c0 = c * uint32_t(kShortChunk);
+        const int stage = int(g_use % uint32_t(kShortStages));
+#if TOPK_TIMELINE
+        const long long tl_w = clock64();
+#endif
+        if (!mbar_wait(&full[stage], (g_use / uint32_t(kShortStages)) & 1u,
+                       timed_out ? 1u : kWaitLimit))
+          timed_out = true;
+        TLS_COUNT(kTlShortWait, clock64() - tl_w);
+        ++g_use;
+        const uint32_t copied = copied_of(c);
+        const float* src = ring + stage * kShortChunk;
+        // sixteen scores a thread: float4 u of the chunk is t + kShortThreads u
+        float x[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t q4 = uint32_t(4 * (t + kShortThreads * u));
+          if (q4 + 4u <= copied) {
+            const float4 v = reinterpret_cast<const float4*>(src)[t + kShortThreads * u];
+            x[4 * u + 0] = v.x;
+            x[4 * u + 1] = v.y;
+            x[4 * u + 2] = v.z;
+            x[4 * u + 3] = v.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t q = q4 + uint32_t(j);
+              x[4 * u + j] = q < copied ? src[q]
+                             : c0 + q < Lu ? __ldcs(row + c0 + q)
+                                           : __int_as_float(0x7FFFFFFF);  // past the end: a NaN
+            }
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t pos = c0 + uint32_t(4 * (t + kShortThreads * (e >> 2)) + (e & 3));
+          const uint32_t bits = __float_as_uint(x[e]);
+          const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
+          saw_nan |= nan && pos < Lu;
+          const uint64_t w = (uint64_t(order_key(bits)) << 32) | uint64_t(~pos);
+          const bool keep = !nan && w > theta;
+          const uint32_t mask = __ballot_sync(0xFFFFFFFFu, keep);
+          if (mask) {
+            int at = 0;
+            if (lane == 0) at = atomicAdd(&st.cnt, __popc(mask));
+            at = __shfl_sync(0xFFFFFFFFu, at, 0);
+            const int j = at + __popc(mask & ((1u << lane) - 1u));
+            if (keep && IN_BOUNDS(j < cap, p.status)) tray[j] = w;
+          }
+        }
+        Blk::sync();  // (the stage is read: it may take the row's next chunk)
+        if (t == 0 && c + uint32_t(kShortStages) < nc) issue(c + uint32_t(kShortStages));
+        admitted += uint32_t(st.cnt - tray_n);  // the words this chunk sent to the tray
+        tray_n = st.cnt;
+        if (tray_n > mark) {
+          TLS_MARK(kTlShortChunks);
+          TLS_COUNT(kTlShortNSelects, 1);
+          // keep the best k of everything seen so far; the threshold rises
+          const uint64_t T = short_select(tray, tray_n, k, st, t, p.status);
+          theta = T - 1ull;
+          tray_n = k;
+          TLS_MARK(kTlShortSelect);
+        }
+      }
+    }
+    TLS_MARK(kTlShortChunks);
+    // the exact best k, sorted, to the row (empty words past the survivors)
+    if (tray_n > k) {
+      short_select(tray, tray_n, k, st, t, p.status);
+      tray_n = k;
+    }
+    const int P = max(next_pow2_dev(max(tray_n, 1)), kShortThreads);
+    for (int j = tray_n + t; j < max(P, k); j += kShortThreads) tray[j] = 0ull;
+    Blk::sync();
+    team_sort_desc<Blk>(tray, P, 2, t);
+    write_row(p, r, tray, t, kShortThreads);
+    if (t == 0) {
+      atomicAdd(&p.sorts[r], 1u);
+      atomicAdd(&p.survivors[r], uint32_t(tray_n));
+      atomicAdd(&p.admitted[r], admitted);
+    }
+    Blk::sync();  // (the tray and the queue word are rewritten for the next row)
+    TLS_MARK(kTlShortEnd);
+  }
+  if (__any_sync(0xFFFFFFFFu, saw_nan) && lane == 0) atomicOr(p.status, TOPK_STATUS_NAN);
+  if (__any_sync(0xFFFFFFFFu, timed_out) && lane == 0) atomicOr(p.status, TOPK_STATUS_TIMEOUT);
+#if TOPK_TIMELINE
+  if (t == 0) {
+    tls[kTlShortTotal - kTlShortRows] = (unsigned long long)(clock64() - tl_c0);
+    for (int q = 0; q < kTlShortEndSlot - kTlShortRows; ++q) TL_SET(kTlShortRows + q, tls[q]);
+  }
+#endif
+#undef TLS_MARK
+#undef TLS_COUNT
+}
+
 }  // namespace
 }  // namespace topk
 
@@ -3256,6 +3571,10 @@ static int launch_select(const float* scores, int32_t rows, int64_t n, int64_t r
     if (cudaGetLastError() != cudaSuccess) return TOPK_ERR_LAUNCH;
     p.order = order;
   }
+  // Many short rows (the queue plan, rows of at most kShortMaxN elements, no
+  // block pool): one CTA per row, several CTAs per SM.
+  const bool short_rows = p.plan == kPlanQueue && n <= kShortMaxN && bmax == nullptr &&
+                          (flags & TOPK_FLAG_TEST_STALL) == 0;
   // Launched with programmatic stream serialization: the grid may start while
   // the stream's previous grid finishes (its set-up and, for the flat plan, its
   // plan and first visiting keys overlap that grid's tail); it reads global
@@ -3270,6 +3589,16 @@ static int launch_select(const float* scores, int32_t rows, int64_t n, int64_t r
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (short_rows) {
+    // resident CTAs per SM as the shared memory allows (227 KB, 1 KB each reserved)
+    const int per_sm = min(kShortCtasPerSm, (227 * 1024) / (short_smem(kp) + 1024 + int(sizeof(ShortState))));
+    const int64_t ctas = int64_t(sms) * (per_sm > 0 ? per_sm : 1);
+    cfg.gridDim = dim3(unsigned(rows < ctas ? rows : ctas));
+    cfg.blockDim = dim3(kShortThreads);
+    cfg.dynamicSmemBytes = size_t(short_smem(kp));
+    if (cudaLaunchKernelEx(&cfg, short_select_kernel, p) != cudaSuccess) return TOPK_ERR_LAUNCH;
+    return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
+  }
   if (cudaLaunchKernelEx(&cfg, topk_select_kernel, p) != cudaSuccess) return TOPK_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_LAUNCH;
 }
