@@ -24,7 +24,11 @@
  * merges (video transcript 3:18-5:45).  A long piece of a row may start from a
  * threshold that a sample of its first units only makes likely; the row's
  * result is checked against it at the end and, if fewer than k scores of the
- * row lie above it, the row is selected again (TOPK_STATUS_RESCAN).
+ * row lie above it, the row is selected again (TOPK_STATUS_RESCAN).  A batch
+ * of at least as many rows as the device has SMs, with rows of at most 65,536
+ * scores, runs the same threshold-and-tray method with one CTA per row and
+ * no split (the causal prefill's shape); results never depend on which path
+ * ran.
  *
  * Memory: every pointer argument is caller-owned.  The library allocates no
  * memory, frees none, keeps no device state between calls and never
