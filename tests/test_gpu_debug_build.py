@@ -65,6 +65,10 @@ def _cases():
     y = rng.standard_normal((300, 20_000)).astype(np.float32)
     lengths = rng.integers(0, 20_001, size=300).astype(np.int32)
     yield "300 rows queue plan", y, lengths, 20_000, 1000, 0, 0
+    yield "300 rows short-row path k2048", y, lengths, 20_000, 2048, 0, 0
+    c = rng.standard_normal((600, 65536)).astype(np.float32)
+    yield "600 causal rows k512 (short-row path)", c, \
+        np.minimum(104 * (np.arange(600) + 1), 65536).astype(np.int32), 65536, 512, 0, 0
     buf = np.full((5, 9003), np.nan, dtype=np.float32)
     buf[:, :9000] = rng.standard_normal((5, 9000))
     yield "misaligned rows", buf, np.array([9000, 8999, 4097, 1025, 3], np.int32), 9000, 300, 0, 0
