@@ -2604,7 +2604,8 @@ __global__ void __launch_bounds__(kPoolSelThreads) pool_select_kernel(
 
 // The short-row kernel (defined below) and its launch shape.
 constexpr int kShortThreads = 256;
-constexpr int kShortChunk = kShortThreads * 16;  // elements a chunk (16 KB: one bulk copy)
+constexpr int kShortPer = 16;                    // scores a thread tests per chunk
+constexpr int kShortChunk = kShortThreads * kShortPer;  // elements a chunk (one bulk copy)
 constexpr int kShortStages = 2;                  // chunk copies in flight per CTA
 constexpr int kShortMaxN = 65536;                // longest row (valid length) of the path
 constexpr int kShortCtasPerSm = 3;               // resident CTAs per SM at most
@@ -3305,10 +3306,10 @@ __global__ void __launch_bounds__(kShortThreads, kShortCtasPerSm) short_select_k
         ++g_use;
         const uint32_t copied = copied_of(c);
         const float* src = ring + stage * kShortChunk;
-        // sixteen scores a thread: float4 u of the chunk is t + kShortThreads u
-        float x[16];
+        // kShortPer scores a thread: float4 u of the chunk is t + kShortThreads u
+        float x[kShortPer];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kShortPer / 4; ++u) {
           const uint32_t q4 = uint32_t(4 * (t + kShortThreads * u));
           if (q4 + 4u <= copied) {
             const float4 v = reinterpret_cast<const float4*>(src)[t + kShortThreads * u];
@@ -3327,7 +3328,7 @@ __global__ void __launch_bounds__(kShortThreads, kShortCtasPerSm) short_select_k
           }
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < kShortPer; ++e) {
           const uint32_t pos = c0 + uint32_t(4 * (t + kShortThreads * (e >> 2)) + (e & 3));
           const uint32_t bits = __float_as_uint(x[e]);
           const bool nan = (bits & 0x7FFFFFFFu) > 0x7F800000u;
