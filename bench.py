@@ -89,6 +89,17 @@ def _kernel_hash() -> str:
     return hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
 
 
+def _kernel_name(rows: int, n: int, pool: bool, sms: int) -> str:
+    """The selection kernel a call runs (the library's routing rule: batches of
+    at least as many rows as SMs with rows of at most 65,536 scores take the
+    short-row kernel)."""
+    if pool:
+        return "topk_select_kernel (+ pool_select_kernel)"
+    if rows >= min(256, sms) and n <= 65536:
+        return "short_select_kernel"
+    return "topk_select_kernel"
+
+
 def _traffic_per_launch(workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it matches the
     current kernel source and workload; else None."""
@@ -283,6 +294,13 @@ def run_gb300(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = D.max_over_ranks(e0.elapsed_time(e1), device=dev)
     e2e_value = world * rows / (e2e_ms / args.steps / 1e3)
+    # the host-to-device copy alone (what the e2e figure spends outside the kernel)
+    e0.record(stream)
+    for _ in range(args.steps):
+        dev_in.copy_(host_pin, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d_ms = e0.elapsed_time(e1) / args.steps
     h2d = host.numel() * 4 + (0 if w.lengths is None else rows * 4)
     d2h = rows * k * 8 + (rows * pool[0] * 4 if pool else 0)
 
@@ -357,13 +375,14 @@ def run_gb300(args, world, rank, local):
             "traffic": traffic,
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
-            "kernel": "topk_select_kernel" + (" (+ pool_select_kernel)" if pool else ""),
+            "kernel": _kernel_name(rows, n, bool(pool), torch.cuda.get_device_properties(dev).multi_processor_count),
             "algorithmic_bytes_per_launch": alg_bytes,
             "avg_launch_ms": round(avg_launch_ms, 5),
         },
         "e2e": {
             "value": round(e2e_value, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms / args.steps, 4), "h2d_copy_ms_per_step": round(h2d_ms, 4),
             "path": "pinned host -> device copy, " + ("topk_select_pool" if pool else "topk_select") +
                     " (C ABI), device -> pinned host",
         },
