@@ -3113,9 +3113,11 @@ __global__ void __launch_bounds__(kPoolSelThreads) queue_order_kernel(
 // thread CTA per row with no role split, several CTAs per SM, rows taken
 // from the shared queue (longest first).  A row of a few units would spend
 // most of the selection kernel's per-piece work (warm start, two-inbox
-// hand-over, piece end) waiting for its selector team; here a row is read in
-// 4096-element chunks (sixteen scores a thread, the next chunk's loads in
-// flight while this one is tested), and its first chunk sets the threshold.
+// hand-over, piece end) waiting for its selector team; here thread 0 copies
+// the row in 4096-element chunks (one cp.async.bulk each) into a two-stage
+// ring, every thread tests its sixteen scores of a chunk, and the row's first
+// chunk, met with an empty threshold, sets the first one through the select.
+// Rows are not visited in a shuffled order: a row is at most sixteen chunks.
 
 struct ShortState {
   uint32_t hist[256];
