@@ -3350,6 +3350,9 @@ __global__ void __launch_bounds__(kShortThreads, kShortCtasPerSm) short_select_k
         if (t == 0 && c + uint32_t(kShortStages) < nc) issue(c + uint32_t(kShortStages));
         admitted += uint32_t(st.cnt - tray_n);  // the words this chunk sent to the tray
         tray_n = st.cnt;
+        // Every thread reads the count before any thread's next appends change
+        // it (the select begins with a barrier of its own): a warp that read it
+        // late would see the next chunk's words and leave the others' barriers.
         if (tray_n > mark) {
           TLS_MARK(kTlShortChunks);
           TLS_COUNT(kTlShortNSelects, 1);
@@ -3358,6 +3361,8 @@ __global__ void __launch_bounds__(kShortThreads, kShortCtasPerSm) short_select_k
           theta = T - 1ull;
           tray_n = k;
           TLS_MARK(kTlShortSelect);
+        } else {
+          Blk::sync();
         }
       }
     }
